@@ -1,0 +1,574 @@
+// gemm.cuh -- block-quantized int8 MMQ on sm_103a tensor cores.
+//
+// Computes out[m,n] = sum_b scale(m,n,b) * I[m,n,b] with the exact per-block integer dot
+// I[m,n,b] = sum_{k in b} xq[m,k] * wq[n,k]  ("A Negative Result on int8 Tensor-Core MMQ", §2;
+// "08 · R1 — int8 MMQ prefill GEMM", §2.1 and §3.2).
+//
+// GB300 design (the pages' kernels target mma.sync on sm_80..sm_121; this one is written for sm_103a):
+//   * sm_103a has no tcgen05 int8 MMA kind, and its legacy int8 mma.sync rate is a small fraction of
+//     the fp16 tensor rate, so the integer codes are converted EXACTLY to fp16 (integers of magnitude
+//     <= 2048 are exact in fp16) and contracted with tcgen05.mma kind::f16 into f32 TMEM
+//     accumulators.  Every product is an integer < 2^14 and every partial sum of one block an integer
+//     < 2^24, so the f32 accumulator holds the exact int32 block dot.
+//   * One CTA computes a 128 (weight rows, MMA M, TMEM lanes) x 128 (tokens, MMA N) tile over all K.
+//     Each 32-k block is contracted into its own TMEM accumulator (4 buffers of 128 columns rotate),
+//     so the tensor core runs ahead while the epilogue warps rescale the previous blocks.
+//   * Warp roles: warps 0-7 epilogue (rescale in registers, store), warps 8-11 producers (load raw
+//     weight blocks and q8_1 codes, unpack to fp16 in 128B-swizzled K-major smem tiles), warp 12
+//     issues the MMAs (one elected thread) and owns the TMEM allocation.
+//   * The f32 scale correction acc += (xd[m,b] * wd[n,b]) * I stays in registers after a tcgen05.ld,
+//     never through a shared-memory round trip of the accumulator ("A Negative Result", §2-§4).
+//   * IQ1_M: the per-16 sub-scale (2s+1) is folded into the fp16 operand together with the sign fold
+//     8g±1 ("CUDA: add IQ1_M to MMQ", Design), giving exact integers |v| <= 135, so one 32-k
+//     accumulator carries both halves and the block scale is xd * d/8.
+//   * W8A8 ("INT8 W8A8 GEMM — Prefill", §1): no per-block scale; the tensor core accumulates 1024-k
+//     chunks (|partial| < 1024*127*128 < 2^24, exact), the epilogue adds them as int32 and applies
+//     out = bf16(((float)I * xs[m]) * ws[n]).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include "mmq_device.cuh"
+
+namespace mmq {
+
+enum WType { WT_Q8_0 = 0, WT_Q4_0 = 1, WT_Q4_K = 2, WT_IQ1_M = 3, WT_W8A8 = 4 };
+enum Mode { MODE_PROD = 0, MODE_DEBUG = 1 };
+
+constexpr int BM = 128;             // weight rows per tile (MMA M, TMEM lanes)
+constexpr int BN = 128;             // tokens per tile (MMA N)
+constexpr int BK = 64;              // k per pipeline stage: one 128-byte swizzle row of fp16
+constexpr int STAGES = 4;           // smem pipeline depth
+constexpr int NACC = 4;             // TMEM accumulators (BN columns each)
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_PROD_WARPS = 4;
+constexpr int PROD_WARP0 = NUM_EPI_WARPS;
+constexpr int MMA_WARP = NUM_EPI_WARPS + NUM_PROD_WARPS;
+constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+constexpr int TMEM_COLS = NACC * BN;  // 512
+
+constexpr int W8A8_CHUNK_K16 = 64;  // 1024-k chunks for the full-K W8A8 dot
+
+constexpr int A_STAGE_BYTES = BM * 128;
+constexpr int B_STAGE_BYTES = BN * 128;
+constexpr int SC_STAGE_FLOATS = 2 * BM + 2 * BM + 2 * BN + 2 * BN;   // wsc, wmn, xd, xs for 2 blocks
+
+struct SmemLayout {
+    static constexpr int a_off = 0;
+    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr int sc_off = b_off + STAGES * B_STAGE_BYTES;
+    static constexpr int orow_off = sc_off + STAGES * SC_STAGE_FLOATS * 4;
+    static constexpr int trow_off = orow_off + BN * 4;
+    static constexpr int bar_off = trow_off + BN * 4;           // 8-byte aligned
+    static constexpr int n_bars = 4 * STAGES + 2 * NACC + 1;
+    static constexpr int misc_off = bar_off + n_bars * 8;       // tmem slot, abort flag
+    static constexpr int total = misc_off + 16;
+    static constexpr int alloc = total + 1024;                  // slack for 1024-byte alignment
+};
+
+struct GemmParams {
+    const uint8_t* W;           // raw weights (expert 0 for MoE); W8A8: int8 [N][K]
+    const int8_t* xq;           // activation codes [M][K]
+    const float4* xds;          // q8_1 (d, s) pairs [M][K/32], read two blocks at a time
+    const float* w8_ws;         // W8A8 per-channel scales [N]
+    const float* w8_xs;         // W8A8 per-token scales [M]
+    void* out;                  // f32 [rows][N] (bf16 for W8A8)
+    int32_t* partials;          // debug: int32 [M][N][groups]
+    long long w_row_bytes;      // bytes per weight row
+    long long w_expert_bytes;   // bytes per expert (MoE)
+    int M, N, K;
+    // MoE routing (null for dense)
+    const int* rowlist;         // (token*slots + slot) grouped by expert
+    const int* work;            // work items: {expert, start, count} triples
+    const int* nwork;           // number of work items
+    int slots;
+};
+
+// ------------------------------------------------------------------------------------------ weight unpack
+// Raw bytes of one weight row for one 64-k stage, as 32-bit words.
+struct RawA {
+    uint32_t w[17];
+};
+
+template <int WT>
+__device__ __forceinline__ void load_raw_a(RawA& r, const uint8_t* row, int s, bool valid) {
+    if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 17; i++) r.w[i] = 0;
+        return;
+    }
+    if constexpr (WT == WT_Q8_0) {            // two 34-byte blocks: 68 bytes at 68*s (4-aligned)
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 68 * s);
+#pragma unroll
+        for (int i = 0; i < 17; i++) r.w[i] = __ldg(p + i);
+    } else if constexpr (WT == WT_Q4_0) {     // two 18-byte blocks: 36 bytes at 36*s
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 36 * s);
+#pragma unroll
+        for (int i = 0; i < 9; i++) r.w[i] = __ldg(p + i);
+    } else if constexpr (WT == WT_Q4_K) {     // 16-byte super-block header + the stage's 32 code bytes
+        const uint8_t* sb = row + 144 * (s >> 2);
+        const uint4 h = __ldg(reinterpret_cast<const uint4*>(sb));
+        const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(sb + 16 + 32 * (s & 3)));
+        const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(sb + 32 + 32 * (s & 3)));
+        r.w[0] = h.x; r.w[1] = h.y; r.w[2] = h.z; r.w[3] = h.w;
+        r.w[4] = c0.x; r.w[5] = c0.y; r.w[6] = c0.z; r.w[7] = c0.w;
+        r.w[8] = c1.x; r.w[9] = c1.y; r.w[10] = c1.z; r.w[11] = c1.w;
+    } else if constexpr (WT == WT_IQ1_M) {    // the stage's 16 code bytes + signs/sub-scales/d (12 bytes)
+        const uint32_t* sb = reinterpret_cast<const uint32_t*>(row + 76 * (s >> 2));
+#pragma unroll
+        for (int i = 0; i < 4; i++) r.w[i] = __ldg(sb + 4 * (s & 3) + i);
+        r.w[4] = __ldg(sb + 16);
+        r.w[5] = __ldg(sb + 17);
+        r.w[6] = __ldg(sb + 18);
+    } else {                                   // W8A8: 64 int8
+        const uint4* p = reinterpret_cast<const uint4*>(row + 64 * s);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint4 v = __ldg(p + i);
+            r.w[4 * i] = v.x; r.w[4 * i + 1] = v.y; r.w[4 * i + 2] = v.z; r.w[4 * i + 3] = v.w;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t byte_shift2(uint32_t a, uint32_t b) {   // bytes 2..5 of {a, b}
+    return __byte_perm(a, b, 0x5432);
+}
+
+// Four unsigned bytes (each 0..255) -> two fp16x2 words of (byte - bias).
+__device__ __forceinline__ void u8x4_to_f16x4(uint32_t u, uint32_t bias_f16x2, uint32_t& lo, uint32_t& hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias_f16x2));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias_f16x2));
+}
+
+__device__ __forceinline__ uint32_t field_le(const uint32_t* words, int pos, int width) {
+    const int wi = pos >> 5, off = pos & 31;
+    const uint32_t v = __funnelshift_r(words[wi], words[wi + 1], off);
+    return v & ((1u << width) - 1u);
+}
+
+// Unpack one row's 64-k stage into 32 fp16x2 words (k order) plus the two blocks' scales.
+// PROD_FOLD: IQ1_M folds (2s+1) into the values (production); debug keeps 8g±1.
+template <int WT, bool PROD_FOLD>
+__device__ __forceinline__ void unpack_a(const RawA& r, int s, uint32_t (&h)[32], float (&wsc)[2], float (&wmn)[2]) {
+    if constexpr (WT == WT_Q8_0) {
+        wsc[0] = half_bits_to_float((uint16_t)(r.w[0] & 0xFFFFu));
+        wsc[1] = half_bits_to_float((uint16_t)(r.w[8] >> 16));
+        wmn[0] = wmn[1] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) s8x4_to_f16x4(byte_shift2(r.w[j], r.w[j + 1]), h[2 * j], h[2 * j + 1]);
+#pragma unroll
+        for (int j = 0; j < 8; j++) s8x4_to_f16x4(r.w[9 + j], h[16 + 2 * j], h[16 + 2 * j + 1]);
+    } else if constexpr (WT == WT_Q4_0) {
+        wsc[0] = half_bits_to_float((uint16_t)(r.w[0] & 0xFFFFu));
+        wsc[1] = half_bits_to_float((uint16_t)(r.w[4] >> 16));
+        wmn[0] = wmn[1] = 0.f;
+        const uint32_t bias = 0x64086408u;                     // 1024 + 8: value = code - 8
+#pragma unroll
+        for (int blk = 0; blk < 2; blk++) {
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint32_t nw = blk == 0 ? byte_shift2(r.w[j], r.w[j + 1]) : r.w[5 + j];
+                const int base = 16 * blk;                     // fp16x2 word index of the block
+                u8x4_to_f16x4(nw & 0x0F0F0F0Fu, bias, h[base + 2 * j], h[base + 2 * j + 1]);
+                u8x4_to_f16x4((nw >> 4) & 0x0F0F0F0Fu, bias, h[base + 8 + 2 * j], h[base + 8 + 2 * j + 1]);
+            }
+        }
+    } else if constexpr (WT == WT_Q4_K) {
+        const float d = half_bits_to_float((uint16_t)(r.w[0] & 0xFFFFu));
+        const float dmin = half_bits_to_float((uint16_t)(r.w[0] >> 16));
+        const uint32_t bits[4] = {r.w[1], r.w[2], r.w[3], 0u};
+        const int j = s & 3;                                   // sub-blocks 2j, 2j+1
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            wsc[i] = d * (float)field_le(bits, 6 * (2 * j + i), 6);
+            wmn[i] = dmin * (float)field_le(bits, 6 * (8 + 2 * j + i), 6);
+        }
+        const uint32_t bias = 0x64006400u;                     // unsigned codes 0..15
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            const uint32_t nw = r.w[4 + t];
+            u8x4_to_f16x4(nw & 0x0F0F0F0Fu, bias, h[2 * t], h[2 * t + 1]);
+            u8x4_to_f16x4((nw >> 4) & 0x0F0F0F0Fu, bias, h[16 + 2 * t], h[16 + 2 * t + 1]);
+        }
+    } else if constexpr (WT == WT_IQ1_M) {
+        const int j = s & 3;
+        const uint32_t signs = (r.w[4] >> (8 * j)) & 0xFFu;    // one bit per 8 values of this stage
+        const uint32_t sbits[3] = {(r.w[5] >> 0), r.w[6] & 0xFFFFu, 0u};   // bytes 68..73 of the block
+        const float d = half_bits_to_float((uint16_t)(r.w[6] >> 16));
+        wsc[0] = wsc[1] = PROD_FOLD ? d * 0.125f : 0.f;
+        wmn[0] = wmn[1] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {                          // 16-value sub-scale groups
+            const int mult = PROD_FOLD ? (int)(2u * field_le(sbits, 3 * (4 * j + q), 3) + 1u) : 1;
+            const uint32_t cw = r.w[q];                        // 16 two-bit codes
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                const int k = 16 * q + e;
+                const int sg0 = ((signs >> (k >> 3)) & 1u) ? -1 : 1;
+                const int g0 = (int)((cw >> (2 * e)) & 3u) - 1;
+                const int g1 = (int)((cw >> (2 * e + 2)) & 3u) - 1;
+                const int v0 = mult * (8 * g0 + sg0);
+                const int v1 = mult * (8 * g1 + sg0);          // e, e+1 share the 8-value sign group
+                const uint32_t pair = (uint32_t)(v0 + 256) | ((uint32_t)(v1 + 256) << 16);
+                h[k >> 1] = u10x2_to_f16x2(pair, 0x65006500u);   // minus (1024 + 256)
+            }
+        }
+    } else {                                                    // W8A8
+        wsc[0] = wsc[1] = 0.f;
+        wmn[0] = wmn[1] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; j++) s8x4_to_f16x4(r.w[j], h[2 * j], h[2 * j + 1]);
+    }
+}
+
+// ------------------------------------------------------------------------------------------ kernel
+template <int WT, int MODE>
+struct KTraits {
+    static constexpr bool kIsW8 = WT == WT_W8A8;
+    // k16 MMA steps per accumulator group
+    static constexpr int G16 = (MODE == MODE_DEBUG) ? ((WT == WT_IQ1_M) ? 1 : 2) : (kIsW8 ? W8A8_CHUNK_K16 : 2);
+    static constexpr bool kScaleRing = (MODE == MODE_PROD) && !kIsW8;
+    static constexpr bool kFold = (MODE == MODE_PROD);
+};
+
+template <int WT, int MODE, bool MOE>
+__global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams p) {
+    using T = KTraits<WT, MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- tile coordinates
+    const int n0 = blockIdx.x * BM;
+    int m0 = blockIdx.y * BN, mcount = min(BN, p.M - m0), expert = 0;
+    if constexpr (MOE) {
+        if ((int)blockIdx.y >= __ldg(p.nwork)) return;        // uniform for the whole CTA
+        const int* wi = p.work + 3 * blockIdx.y;
+        expert = __ldg(wi);
+        m0 = __ldg(wi + 1);
+        mcount = __ldg(wi + 2);
+    }
+    const uint8_t* Wbase = p.W + (long long)expert * p.w_expert_bytes;
+
+    float* sc_base = reinterpret_cast<float*>(smem + SmemLayout::sc_off);
+    int* orow = reinterpret_cast<int*>(smem + SmemLayout::orow_off);
+    int* trow = reinterpret_cast<int*>(smem + SmemLayout::trow_off);
+    const uint32_t bar0 = smem_u32(smem + SmemLayout::bar_off);
+    auto bar_full = [&](int i) { return bar0 + 8u * i; };
+    auto bar_empty = [&](int i) { return bar0 + 8u * (STAGES + i); };
+    auto bar_sfull = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
+    auto bar_sfree = [&](int i) { return bar0 + 8u * (3 * STAGES + i); };
+    auto bar_accf = [&](int i) { return bar0 + 8u * (4 * STAGES + i); };
+    auto bar_acce = [&](int i) { return bar0 + 8u * (4 * STAGES + NACC + i); };
+    const uint32_t bar_done = bar0 + 8u * (4 * STAGES + 2 * NACC);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+
+    // ---- setup: barriers, TMEM, row maps
+    if (warp == MMA_WARP) {
+        if (lane == 0) {
+            for (int i = 0; i < STAGES; i++) {
+                mbar_init(bar_full(i), NUM_PROD_WARPS * 32);
+                mbar_init(bar_empty(i), 1);
+                mbar_init(bar_sfull(i), NUM_PROD_WARPS * 32);
+                mbar_init(bar_sfree(i), NUM_EPI_WARPS);
+            }
+            for (int i = 0; i < NACC; i++) {
+                mbar_init(bar_accf(i), 1);
+                mbar_init(bar_acce(i), NUM_EPI_WARPS);
+            }
+            mbar_init(bar_done, 1);
+            *abort_flag = 0;
+            fence_barrier_init();
+        }
+        __syncwarp();
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x < BN) {
+        const int j = threadIdx.x;
+        int tr = -1, orr = -1;
+        if (j < mcount) {
+            if constexpr (MOE) {
+                const int rl = __ldg(p.rowlist + m0 + j);
+                tr = rl / p.slots;
+                orr = rl;
+            } else {
+                tr = m0 + j;
+                orr = m0 + j;
+            }
+        }
+        trow[j] = tr;
+        orow[j] = orr;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int nstages = p.K / BK;
+    const int nk16 = p.K / 16;
+    const int ngroups = (nk16 + T::G16 - 1) / T::G16;
+    const int kb32 = p.K / 32;
+
+    if (warp >= PROD_WARP0 && warp < MMA_WARP) {
+        // =========================================================== producers
+        const int r = threadIdx.x - PROD_WARP0 * 32;            // row of A and of B this thread fills
+        const int n = n0 + r;
+        const bool a_valid = n < p.N;
+        const uint8_t* arow = Wbase + (long long)(a_valid ? n : 0) * p.w_row_bytes;
+        const int tr = trow[r];
+        const bool b_valid = tr >= 0;
+        const int8_t* brow = p.xq + (long long)(b_valid ? tr : 0) * p.K;
+        const float4* bds = p.xds + (long long)(b_valid ? tr : 0) * (kb32 / 2);
+        const uint32_t a_smem = smem_u32(smem + SmemLayout::a_off);
+        const uint32_t b_smem = smem_u32(smem + SmemLayout::b_off);
+
+        // Two register sets of raw bytes: the loads for stage s+1 are in flight while stage s is
+        // unpacked and stored.
+        struct RawSet {
+            RawA a;
+            uint4 b[4];
+            float4 ds;
+        };
+        auto load_stage = [&](RawSet& rs, int s) {
+            load_raw_a<WT>(rs.a, arow, s, a_valid);
+            if (b_valid) {
+                const uint4* qp = reinterpret_cast<const uint4*>(brow + 64 * s);
+#pragma unroll
+                for (int i = 0; i < 4; i++) rs.b[i] = __ldg(qp + i);
+                if constexpr (T::kScaleRing) rs.ds = __ldg(bds + s);
+                else rs.ds = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; i++) rs.b[i] = make_uint4(0u, 0u, 0u, 0u);
+                rs.ds = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        };
+        auto produce = [&](RawSet& rs, int s) {
+            const int slot = s % STAGES;
+            const uint32_t par = ((s / STAGES) & 1) ^ 1;
+            mbar_wait(bar_empty(slot), par, abort_flag);
+            if constexpr (T::kScaleRing) mbar_wait(bar_sfree(slot), par, abort_flag);
+            const uint32_t at = a_smem + slot * A_STAGE_BYTES;
+            const uint32_t bt = b_smem + slot * B_STAGE_BYTES;
+            {
+                uint32_t ha[32];
+                float wsc[2], wmn[2];
+                unpack_a<WT, T::kFold>(rs.a, s, ha, wsc, wmn);
+                if (!a_valid) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    st_shared_v4(at + sw128_off(r, c), ha[4 * c], ha[4 * c + 1], ha[4 * c + 2], ha[4 * c + 3]);
+                if constexpr (T::kScaleRing) {
+                    float* sc = sc_base + slot * SC_STAGE_FLOATS;
+                    sc[0 * BM + r] = wsc[0];
+                    sc[1 * BM + r] = wsc[1];
+                    sc[2 * BM + r] = wmn[0];
+                    sc[3 * BM + r] = wmn[1];
+                    sc[4 * BM + r] = rs.ds.x;                 // xd, block 0
+                    sc[4 * BM + BN + r] = rs.ds.z;            // xd, block 1
+                    sc[4 * BM + 2 * BN + r] = rs.ds.y;        // xs, block 0
+                    sc[4 * BM + 3 * BN + r] = rs.ds.w;        // xs, block 1
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                uint32_t hb[8];
+                s8x4_to_f16x4(rs.b[i].x, hb[0], hb[1]);
+                s8x4_to_f16x4(rs.b[i].y, hb[2], hb[3]);
+                s8x4_to_f16x4(rs.b[i].z, hb[4], hb[5]);
+                s8x4_to_f16x4(rs.b[i].w, hb[6], hb[7]);
+                st_shared_v4(bt + sw128_off(r, 2 * i), hb[0], hb[1], hb[2], hb[3]);
+                st_shared_v4(bt + sw128_off(r, 2 * i + 1), hb[4], hb[5], hb[6], hb[7]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_full(slot));
+            if constexpr (T::kScaleRing) mbar_arrive(bar_sfull(slot));
+        };
+
+        RawSet set0, set1;
+        load_stage(set0, 0);
+        if (nstages > 1) load_stage(set1, 1);
+        for (int s = 0; s < nstages; s += 2) {
+            produce(set0, s);
+            if (s + 2 < nstages) load_stage(set0, s + 2);
+            if (s + 1 < nstages) {
+                produce(set1, s + 1);
+                if (s + 3 < nstages) load_stage(set1, s + 3);
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        // =========================================================== MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(BM, BN);
+            const uint32_t a_smem = smem_u32(smem + SmemLayout::a_off);
+            const uint32_t b_smem = smem_u32(smem + SmemLayout::b_off);
+            for (int s = 0; s < nstages && !*abort_flag; s++) {
+                const int slot = s % STAGES;
+                if (!mbar_wait(bar_full(slot), (s / STAGES) & 1, abort_flag)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const int ks = 4 * s + j;
+                    const int kin = ks % T::G16;
+                    const int g = ks / T::G16;
+                    const int buf = g % NACC;
+                    if (kin == 0) {
+                        mbar_wait(bar_acce(buf), ((g / NACC) & 1) ^ 1, abort_flag);
+                        tc_fence_after();
+                    }
+                    const uint64_t ad = sdesc_sw128(a_smem + slot * A_STAGE_BYTES + 32 * j);
+                    const uint64_t bd = sdesc_sw128(b_smem + slot * B_STAGE_BYTES + 32 * j);
+                    umma_f16(tmem_base + buf * BN, ad, bd, idesc, kin != 0 ? 1u : 0u);
+                    if (kin == T::G16 - 1 || ks == nk16 - 1) umma_commit(bar_accf(buf));
+                }
+                umma_commit(bar_empty(slot));
+            }
+            // every MMA and every commit-arrive of this CTA has landed once this barrier flips
+            umma_commit(bar_done);
+            mbar_wait_final(bar_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // =========================================================== epilogue
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int ch = warp >> 2;               // column half: tokens 64*ch .. 64*ch+63
+        const int r = 32 * q + lane;            // tile row (weight row n0 + r)
+        const int n = n0 + r;
+        const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + 64 * ch;
+
+        float acc[(MODE == MODE_PROD && !T::kIsW8) ? 64 : 1];
+        int32_t iacc[T::kIsW8 ? 64 : 1];
+#pragma unroll
+        for (int j = 0; j < (int)(sizeof(acc) / sizeof(float)); j++) acc[j] = 0.f;
+        if constexpr (T::kIsW8) {
+#pragma unroll
+            for (int j = 0; j < 64; j++) iacc[j] = 0;
+        }
+
+        for (int g = 0; g < ngroups; g++) {
+            const int buf = g % NACC;
+            mbar_wait(bar_accf(buf), (g / NACC) & 1, abort_flag);
+            tc_fence_after();
+            const float* sc = nullptr;
+            float rs = 0.f, mn = 0.f;
+            int slot = 0, i = 0;
+            if constexpr (T::kScaleRing) {
+                const int s = g >> 1;
+                i = g & 1;
+                slot = s % STAGES;
+                if (i == 0) mbar_wait(bar_sfull(slot), (s / STAGES) & 1, abort_flag);
+                sc = sc_base + slot * SC_STAGE_FLOATS;
+                rs = sc[i * BM + r];
+                if constexpr (WT == WT_Q4_K) mn = sc[2 * BM + i * BM + r];
+            }
+            // two halves of 32 columns: load, then rescale, so only 32 partials are live at a time
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                uint32_t v[32];
+                tmem_ld32(tbase + buf * BN + 32 * hh, v);
+                tmem_ld_wait();
+                if (hh == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acce(buf));
+                }
+                if constexpr (MODE == MODE_DEBUG) {
+                    if (n < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) {
+                            const int col = 64 * ch + 32 * hh + j;
+                            if (col < mcount)
+                                p.partials[((long long)(m0 + col) * p.N + n) * ngroups + g] =
+                                    __float2int_rn(__uint_as_float(v[j]));
+                        }
+                    }
+                } else if constexpr (T::kIsW8) {
+#pragma unroll
+                    for (int j = 0; j < 32; j++) iacc[32 * hh + j] += __float2int_rn(__uint_as_float(v[j]));
+                } else {
+                    const float* xd = sc + 4 * BM + i * BN + 64 * ch + 32 * hh;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 c = *reinterpret_cast<const float4*>(xd + j);
+                        acc[32 * hh + j + 0] = fmaf(__uint_as_float(v[j + 0]), rs * c.x, acc[32 * hh + j + 0]);
+                        acc[32 * hh + j + 1] = fmaf(__uint_as_float(v[j + 1]), rs * c.y, acc[32 * hh + j + 1]);
+                        acc[32 * hh + j + 2] = fmaf(__uint_as_float(v[j + 2]), rs * c.z, acc[32 * hh + j + 2]);
+                        acc[32 * hh + j + 3] = fmaf(__uint_as_float(v[j + 3]), rs * c.w, acc[32 * hh + j + 3]);
+                    }
+                    if constexpr (WT == WT_Q4_K) {
+                        const float* xs = sc + 4 * BM + 2 * BN + i * BN + 64 * ch + 32 * hh;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 c = *reinterpret_cast<const float4*>(xs + j);
+                            acc[32 * hh + j + 0] = fmaf(-mn, c.x, acc[32 * hh + j + 0]);
+                            acc[32 * hh + j + 1] = fmaf(-mn, c.y, acc[32 * hh + j + 1]);
+                            acc[32 * hh + j + 2] = fmaf(-mn, c.z, acc[32 * hh + j + 2]);
+                            acc[32 * hh + j + 3] = fmaf(-mn, c.w, acc[32 * hh + j + 3]);
+                        }
+                    }
+                }
+            }
+            if constexpr (T::kScaleRing) {
+                if (i == 1 || g == ngroups - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_sfree(slot));
+                }
+            }
+        }
+
+        // ---- store
+        if constexpr (MODE == MODE_PROD) {
+            if (n < p.N) {
+                const int* orw = orow + 64 * ch;
+                if constexpr (T::kIsW8) {
+                    const float wsn = __ldg(p.w8_ws + n);
+                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+                    for (int j = 0; j < 64; j++) {
+                        const int orr = orw[j];
+                        if (orr >= 0) {
+                            const float t = __fmul_rn((float)iacc[j], __ldg(p.w8_xs + orr));
+                            out[(long long)orr * p.N + n] = __float2bfloat16_rn(__fmul_rn(t, wsn));
+                        }
+                    }
+                } else {
+                    float* out = reinterpret_cast<float*>(p.out);
+#pragma unroll
+                    for (int j = 0; j < 64; j++) {
+                        const int orr = orw[j];
+                        if (orr >= 0) out[(long long)orr * p.N + n] = acc[j];
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------------------------ host launch
+template <int WT, int MODE, bool MOE>
+cudaError_t launch_gemm(const GemmParams& p, int grid_y, cudaStream_t stream) {
+    static bool configured = false;
+    auto kern = mmq_gemm_kernel<WT, MODE, MOE>;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::alloc);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    dim3 grid((p.N + BM - 1) / BM, grid_y);
+    kern<<<grid, NTHREADS, SmemLayout::alloc, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace mmq

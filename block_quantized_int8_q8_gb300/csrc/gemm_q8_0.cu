@@ -1,0 +1,15 @@
+// gemm_q8_0.cu -- instantiation of the MMQ tensor-core kernel for one weight type (see gemm.cuh).
+#include "gemm.cuh"
+#include "internal.h"
+
+namespace mmq {
+
+cudaError_t run_gemm_q8_0(const GemmParams& p, int mode, bool moe, int grid_y, cudaStream_t s) {
+    if (mode == MODE_DEBUG) return launch_gemm<WT_Q8_0, MODE_DEBUG, false>(p, grid_y, s);
+    if (moe) return launch_gemm<WT_Q8_0, MODE_PROD, true>(p, grid_y, s);
+    return launch_gemm<WT_Q8_0, MODE_PROD, false>(p, grid_y, s);
+}
+
+MMQ_DEFINE_ERROR_READER(q8_0)
+
+}  // namespace mmq

@@ -1,0 +1,55 @@
+// internal.h -- host-side interface between the C ABI (capi.cu) and the kernel translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mmq {
+struct GemmParams;
+
+// Quantizer (quantize.cu)
+cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq, cudaStream_t s);
+
+// Dense / MoE / debug GEMM launchers, one per weight type (gemm_<type>.cu).
+// mode: 0 production, 1 debug partials.  moe: grouped launch driven by the routing workspace.
+cudaError_t run_gemm_q8_0(const GemmParams& p, int mode, bool moe, int grid_y, cudaStream_t s);
+cudaError_t run_gemm_q4_0(const GemmParams& p, int mode, bool moe, int grid_y, cudaStream_t s);
+cudaError_t run_gemm_q4_k(const GemmParams& p, int mode, bool moe, int grid_y, cudaStream_t s);
+cudaError_t run_gemm_iq1_m(const GemmParams& p, int mode, bool moe, int grid_y, cudaStream_t s);
+cudaError_t run_gemm_w8a8(const GemmParams& p, int mode, bool moe, int grid_y, cudaStream_t s);
+
+// MoE routing (route.cu): count, scan into work items, scatter.  Workspace carved by the caller.
+struct RouteWorkspace {
+    int* counts;     // [E]
+    int* offsets;    // [E]
+    int* cursor;     // [E]
+    int* nwork;      // [1]
+    int* work;       // [3 * max_work]
+    int* rowlist;    // [M * slots]
+    int max_work;
+};
+cudaError_t run_route(const int32_t* ids, int M, int slots, int E, int tile_n, const RouteWorkspace& ws,
+                      cudaStream_t s);
+
+// Per-translation-unit device error words: read, OR into *bits, clear.
+cudaError_t read_clear_errors_quantize(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_route(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_q8_0(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_q4_0(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_q4_k(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_iq1_m(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_w8a8(unsigned* bits, cudaStream_t s);
+}  // namespace mmq
+
+// Defines read_clear_errors_<name> for the translation unit that expands it.
+#define MMQ_DEFINE_ERROR_READER(name)                                                               \
+    cudaError_t read_clear_errors_##name(unsigned* bits, cudaStream_t s) {                          \
+        unsigned v = 0, z = 0;                                                                      \
+        cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_mmq_device_errors, sizeof(v), 0,            \
+                                                  cudaMemcpyDeviceToHost, s);                       \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);                                         \
+        if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_mmq_device_errors, &z, sizeof(z), 0,    \
+                                                          cudaMemcpyHostToDevice, s);               \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);                                         \
+        *bits |= v;                                                                                 \
+        return e;                                                                                   \
+    }

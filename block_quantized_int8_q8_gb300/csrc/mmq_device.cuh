@@ -1,0 +1,194 @@
+// mmq_device.cuh -- sm_103a device primitives for the MMQ kernels: mbarriers with bounded waits,
+// tcgen05 (TMEM allocation, MMA, commit, loads), shared-memory matrix descriptors, fp16 packing.
+//
+// Every wait in this library is bounded: after MMQ_WAIT_LIMIT_CYCLES of SM clock the waiting thread
+// records MMQ_DEVERR_TIMEOUT in the device error word, raises the CTA's abort flag and returns, and
+// every later wait in the CTA returns at once, so a broken pipeline ends the kernel instead of
+// hanging the GPU.  TMEM is always released before the CTA exits.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace mmq {
+
+// Device-resident error word (MMQ_DEVERR_* bits), one per translation unit; the C ABI reads and
+// clears every unit's word in mmq_read_device_errors.
+static __device__ unsigned g_mmq_device_errors;
+
+constexpr long long MMQ_WAIT_LIMIT_CYCLES = 4000000000ll;   // ~2 s at GB300 clocks
+constexpr unsigned DEVERR_TIMEOUT = 1u;
+constexpr unsigned DEVERR_EXPERT_ID = 2u;
+constexpr unsigned DEVERR_DUP_EXPERT = 4u;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.release.cta.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Bounded: returns false (and sets the
+// abort flag and the device error word) when the limit is exceeded or the CTA already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > MMQ_WAIT_LIMIT_CYCLES) {
+            *abort_flag = 1;
+            atomicOr(&g_mmq_device_errors, DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Wait bounded by time only (ignores the abort flag): used before teardown so that no asynchronous
+// arrive can land after the CTA's shared memory is released.
+__device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > MMQ_WAIT_LIMIT_CYCLES) {
+            atomicOr(&g_mmq_device_errors, DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor core).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 operands, f32 accumulation), issued by one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on an mbarrier when all previously issued tcgen05 async operations of this thread
+// have completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B fp16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4)                               // D format: f32
+           | (0u << 7) | (0u << 10)                // A, B format: f16
+           | (0u << 15) | (0u << 16)               // A, B K-major
+           | ((uint32_t)(N >> 3) << 17)            // N / 8
+           | ((uint32_t)(M >> 4) << 24);           // M / 16
+}
+
+// Shared-memory matrix descriptor for a K-major operand stored with the 128-byte swizzle: rows of
+// 128 bytes (64 fp16), 8-row groups 1024 bytes apart, tile base 1024-byte aligned.  Advancing the
+// start address by 32 bytes selects the next 16-element K slice inside the swizzle atom.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                           // fixed 0b001 field
+    d |= (uint64_t)2 << 61;                           // swizzle mode: 128 B
+    return d;
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128B-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
+    return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// 32 columns of 32-bit TMEM values for this warp's 32 lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------------------------------ fp16 packing
+// Exact small-integer -> fp16 conversion by exponent splicing: the fp16 pattern 0x6400 | b is
+// 1024 + b for 0 <= b < 1024, so subtracting (1024 + bias) in fp16 gives b - bias exactly.
+
+// Four signed int8 (one 32-bit word, little-endian) -> two fp16x2 words, in order.
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;                       // b + 128 in 0..255
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    const uint32_t bias = 0x64806480u;                        // (1152, 1152) = 1024 + 128
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
+// Two unsigned values 0..1023 already placed at bits [0,10) and [16,26) -> fp16x2 of (v - bias).
+__device__ __forceinline__ uint32_t u10x2_to_f16x2(uint32_t pair, uint32_t bias_f16x2) {
+    uint32_t r;
+    const uint32_t h = pair | 0x64006400u;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(bias_f16x2));
+    return r;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+}  // namespace mmq

@@ -1,0 +1,91 @@
+// quantize.cu -- q8_1 activation quantizer for sm_103a.
+//
+// Per 32-value block: amax = max|x|, d = amax/127, q = round-half-even(x/d) (correctly rounded f32
+// division), s = d * sum(q)  ("08 · R1 — int8 MMQ prefill GEMM", §2.2 q8_1 activation pipeline, and
+// the §3.2 reference quantizer; f32 scale, the block sum produced in the same pass).
+// Output layout: int8 q[M][K] at byte 0, then float2 (d, s)[M][K/32].
+//
+// HBM-bound: 4 bytes read and 1.25 bytes written per value.  Eight lanes own one block (one float4
+// each); amax and sum(q) are warp-shuffle reductions over the eight lanes; every lane stores its
+// four codes as one 32-bit word, so a warp writes 128 contiguous bytes per block quad.
+#include <cstdint>
+#include "internal.h"
+#include "mmq_device.cuh"
+
+namespace mmq {
+
+constexpr int QZ_UNROLL = 4;      // blocks per 8-lane group per iteration (loads in flight)
+
+__device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ int q8_code(float x, float d) {
+    const int q = __float2int_rn(__fdiv_rn(x, d));        // ties to even
+    return max(-127, min(127, q));
+}
+
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, uint32_t* __restrict__ q,
+                                                           float2* __restrict__ ds, long long nblk) {
+    const int lane = threadIdx.x & 31, sub = lane & 7, grp = lane >> 3;
+    const long long warp_id = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = (gridDim.x * (long long)blockDim.x) >> 5;
+    // one warp iteration covers 4 groups x QZ_UNROLL blocks
+    for (long long base = warp_id * 4 * QZ_UNROLL; base < nblk; base += nwarps * 4 * QZ_UNROLL) {
+        float4 v[QZ_UNROLL];
+#pragma unroll
+        for (int u = 0; u < QZ_UNROLL; u++) {
+            const long long blk = base + u * 4 + grp;
+            v[u] = blk < nblk ? ld_stream_f4(x + blk * 8 + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < QZ_UNROLL; u++) {
+            const long long blk = base + u * 4 + grp;
+            float a = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            const float d = __fdiv_rn(a, 127.0f);
+            int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+            if (d != 0.0f) {
+                q0 = q8_code(v[u].x, d);
+                q1 = q8_code(v[u].y, d);
+                q2 = q8_code(v[u].z, d);
+                q3 = q8_code(v[u].w, d);
+            }
+            int sum = q0 + q1 + q2 + q3;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if (blk < nblk) {
+                q[blk * 8 + sub] = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
+                                   ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
+                if (sub == 0) ds[blk] = make_float2(d, __fmul_rn(d, (float)sum));
+            }
+        }
+    }
+}
+
+cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq, cudaStream_t s) {
+    const long long nblk = M * K / 32;
+    if (nblk == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long warps_needed = (nblk + 4 * QZ_UNROLL - 1) / (4 * QZ_UNROLL);
+    long long blocks = (warps_needed + 7) / 8;
+    const long long cap = (long long)sms * 8;              // 8 x 256 threads resident per SM
+    if (blocks > cap) blocks = cap;
+    uint8_t* base = static_cast<uint8_t*>(xq);
+    quantize_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(x),
+                                                          reinterpret_cast<uint32_t*>(base),
+                                                          reinterpret_cast<float2*>(base + M * K), nblk);
+    return cudaGetLastError();
+}
+
+MMQ_DEFINE_ERROR_READER(quantize)
+
+}  // namespace mmq

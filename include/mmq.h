@@ -84,6 +84,10 @@ typedef enum {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mmq_status_string(mmq_status s);
 
+/* Name and description of the CUDA error behind the most recent MMQ_ERR_CUDA returned on the calling
+ * host thread ("" if none).  The string stays valid until the next failing call on that thread. */
+const char* mmq_last_cuda_error(void);
+
 /* Bytes of a q8_1 activation buffer for an [M][K] matrix: 40*M*K/32. */
 size_t mmq_q8_1_bytes(int64_t M, int64_t K);
 

@@ -1,0 +1,70 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every symbol the header
+declares, computes the documented buffer sizes, and rejects bad arguments synchronously (status codes
+are returned before any CUDA call is made, so fake pointers are safe here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_quantized_int8_q8_gb300 import _build, api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return api.load()
+
+
+def test_header_declares_exactly_the_exported_api(lib):
+    header = open(os.path.join(ROOT, "include", "mmq.h")).read()
+    declared = set(re.findall(r"\b(mmq_[a-z0-9_]+)\s*\(", header))
+    assert declared == set(api.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_sizes(lib):
+    assert api.q8_1_bytes(3, 64) == 3 * 64 + 3 * 2 * 8
+    assert api.weight_bytes(api.Q8_0, 5, 256) == 5 * 8 * 34
+    assert api.weight_bytes(api.Q4_0, 5, 256) == 5 * 8 * 18
+    assert api.weight_bytes(api.Q4_K, 5, 512) == 5 * 2 * 144
+    assert api.weight_bytes(api.IQ1_M, 5, 512) == 5 * 2 * 76
+    assert api.weight_bytes(api.W8A8, 5, 64) == 5 * 64 + 20
+    assert api.weight_bytes(api.Q4_K, 5, 100) == 0
+    assert api.w8a8_act_bytes(7, 64) == 7 * 64 + 28
+    assert api.gemm_id_workspace_bytes(512, 8, 64) > 512 * 8 * 4
+
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced: every case fails validation first
+
+
+@pytest.mark.parametrize("args,status", [
+    ((api.Q4_0, FAKE, FAKE, FAKE, 4, 4, 100), 2),        # K not a multiple of 256
+    ((api.Q4_0, FAKE, FAKE, FAKE, -1, 4, 256), 2),       # negative M
+    ((api.W8A8, FAKE, FAKE, FAKE, 4, 4, 96), 2),         # W8A8 K % 64
+    ((7, FAKE, FAKE, FAKE, 4, 4, 256), 1),               # unknown type
+    ((api.Q4_0, None, FAKE, FAKE, 4, 4, 256), 1),        # null weights
+    ((api.Q4_0, FAKE + 4, FAKE, FAKE, 4, 4, 256), 3),    # misaligned
+    ((api.Q4_0, FAKE, FAKE, FAKE, 1 << 20, 1 << 12, 1 << 12), 2),   # M*K beyond int32
+])
+def test_gemm_argument_validation(lib, args, status):
+    assert lib.mmq_gemm(*args, None) == status
+
+
+def test_quantize_and_gemm_id_validation(lib):
+    assert lib.mmq_quantize_q8_1(FAKE, 4, 33, FAKE, None) == 2
+    assert lib.mmq_quantize_q8_1(None, 4, 32, FAKE, None) == 1
+    assert lib.mmq_quantize_q8_1(FAKE, 4, 32, FAKE + 8, None) == 3
+    ok = (api.IQ1_M, FAKE, 4, FAKE, FAKE, 2, FAKE, 16, 128, 256)
+    need = api.gemm_id_workspace_bytes(16, 2, 4)
+    assert lib.mmq_gemm_id(*ok, FAKE, need - 1, None) == 6          # workspace too small
+    assert lib.mmq_gemm_id(*ok, None, need, None) == 6
+    assert lib.mmq_gemm_id(api.W8A8, *ok[1:], FAKE, need, None) == 4
+    assert lib.mmq_gemm_id(api.IQ1_M, FAKE, 0, *ok[3:], FAKE, need, None) == 1
+    assert lib.mmq_gemm_debug_partials(api.Q4_K, FAKE, FAKE, FAKE, 4, 4, 128, None) == 2
+    for s in range(7):
+        assert lib.mmq_status_string(s)
+    assert lib.mmq_read_device_errors(None, None) == 1

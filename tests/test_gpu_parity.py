@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Bars (BASELINE the benchmark spec): q8_1 codes, scales and block sums bit-exact; per-group integer partials
+bit-exact; W8A8 bf16 outputs bit-exact; f32 outputs within max|diff| <= 1e-3 * max|oracle output|.
+Shapes span several 128x128 tiles with ragged M and N tails, plus the degenerate sizes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_quantized_int8_q8_gb300 import api, synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+BLOCK_TYPES = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M]
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    api.load()
+    yield
+    assert api.read_device_errors() == 0
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _rel_err(got, ref):
+    scale = np.abs(ref).max()
+    return float(np.abs(got.astype(np.float64) - ref).max() / (scale if scale > 0 else 1.0))
+
+
+def _oracle_acts(pb):
+    q, d, s = oracle.quantize_q8_1(pb.x)
+    return q, d, s, api.pack_q8_1(torch.from_numpy(q), torch.from_numpy(d), torch.from_numpy(s)).to(DEV)
+
+
+# ---------------------------------------------------------------------------------------- quantizer
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 64), (37, 4096), (257, 1024), (2048, 4096)])
+def test_quantizer_bit_exact(M, K):
+    g = np.random.default_rng(M * 7 + K)
+    x = g.standard_normal((M, K), dtype=np.float32)
+    x[0, :32] = 0.0                                      # an all-zero block
+    if K >= 64:
+        x[0, 32:64] = 0.0
+        x[0, 32] = 127.0
+        x[0, 33:41] = [2.5, 3.5, -2.5, -0.5, 0.5, 1.5, 126.5, -127.0]   # exact ties at d = 1
+    q, d, s = oracle.quantize_q8_1(x)
+    buf = api.quantize_q8_1(_dev(x))
+    torch.cuda.synchronize()
+    qg, dsg = api.q8_1_views(buf, M, K)
+    assert np.array_equal(qg.cpu().numpy(), q)
+    assert np.array_equal(dsg[..., 0].cpu().numpy().view(np.uint32), d.view(np.uint32))
+    assert np.array_equal(dsg[..., 1].cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+def test_quantizer_extreme_scales_bit_exact():
+    g = np.random.default_rng(3)
+    x = (g.standard_normal((64, 512)) * 10.0 ** g.integers(-30, 30, size=(64, 1))).astype(np.float32)
+    q, d, s = oracle.quantize_q8_1(x)
+    qg, dsg = api.q8_1_views(api.quantize_q8_1(_dev(x)), 64, 512)
+    assert np.array_equal(qg.cpu().numpy(), q)
+    assert np.array_equal(dsg[..., 0].cpu().numpy().view(np.uint32), d.view(np.uint32))
+    assert np.array_equal(dsg[..., 1].cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------------------- block GEMM
+SHAPES = [(1, 1, 256), (5, 130, 256), (130, 257, 512), (200, 300, 1024), (256, 384, 2048), (64, 128, 5376)]
+
+
+@pytest.mark.parametrize("wtype", BLOCK_TYPES)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_block_gemm_matches_oracle(wtype, shape):
+    M, N, K = shape
+    pb = synth.make_problem(wtype, M, N, K, seed=11 + M + N + K + wtype)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm(wtype, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    ref = oracle.gemm(wtype, pb.W, q, d, s, N)
+    assert _rel_err(out, ref) <= TOL
+
+
+@pytest.mark.parametrize("wtype", BLOCK_TYPES + [synth.W8A8])
+@pytest.mark.parametrize("shape", [(3, 5, 256), (131, 200, 512)])
+def test_debug_partials_bit_exact(wtype, shape):
+    M, N, K = shape
+    pb = synth.make_problem(wtype, M, N, K, seed=21 + M + wtype)
+    if wtype == synth.W8A8:
+        xq = _dev(synth.pack_w8a8_acts(pb.X, pb.xs))
+        P = api.gemm_debug_partials(wtype, _dev(pb.W), xq, M, N, K).cpu().numpy()
+        ref = oracle.partials(synth.W8A8, pb.X, pb.fields.W)
+    else:
+        q, d, s, xq = _oracle_acts(pb)
+        P = api.gemm_debug_partials(wtype, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
+        wq, _, _ = oracle.decode(wtype, pb.W, N, K)
+        ref = oracle.partials(wtype, q, wq)
+    assert np.array_equal(P, ref)
+
+
+def test_partials_exact_at_the_block_bound():
+    # every product at its maximum magnitude: block dots of +-32*127*127 must come out exact
+    M, N, K = 130, 130, 512
+    f = synth.draw_fields(np.random.default_rng(1), synth.Q8_0, N, K)
+    f.q[...] = np.where(np.arange(N)[:, None] % 2 == 0, 127, -127).astype(np.int8)
+    W = synth.pack(synth.Q8_0, f)
+    q = np.where(np.arange(M)[:, None] % 3 == 0, -127, 127).astype(np.int8) * np.ones((M, K), np.int8)
+    d = np.ones((M, K // 32), np.float32)
+    xq = api.pack_q8_1(torch.from_numpy(q), torch.from_numpy(d), torch.from_numpy(d)).to(DEV)
+    P = api.gemm_debug_partials(synth.Q8_0, _dev(W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    ref = oracle.partials(synth.Q8_0, q, f.q)
+    assert np.abs(ref).max() == 32 * 127 * 127
+    assert np.array_equal(P, ref)
+
+
+# ---------------------------------------------------------------------------------------- W8A8
+@pytest.mark.parametrize("shape", [(1, 1, 64), (70, 200, 576), (300, 260, 4096)])
+def test_w8a8_bit_exact(shape):
+    M, N, K = shape
+    pb = synth.make_problem(synth.W8A8, M, N, K, seed=31 + M)
+    out = api.gemm(synth.W8A8, _dev(pb.W), _dev(synth.pack_w8a8_acts(pb.X, pb.xs)), M, N, K)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.w8a8(pb.fields.W, pb.fields.ws, pb.X, pb.xs)
+    assert np.array_equal(got, ref)
+
+
+def test_w8a8_exact_at_the_int32_range():
+    # all products +-127*127 over K = 4096: |I| = 66 064 384 > 2^24, exact only with chunked accumulation
+    M, N, K = 130, 129, 4096
+    X = np.where(np.arange(M)[:, None] % 2 == 0, 127, -127).astype(np.int8) * np.ones((M, K), np.int8)
+    W = np.full((N, K), 127, np.int8)
+    W[1::3] = -127
+    W[2::3, ::2] = 0
+    xs = np.ones(M, np.float32)
+    ws = np.ones(N, np.float32)
+    out = api.gemm(synth.W8A8, _dev(synth.pack(synth.W8A8, synth.W8A8Fields(W=W, ws=ws))),
+                   _dev(synth.pack_w8a8_acts(X, xs)), M, N, K)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.w8a8(W, ws, X, xs))
+
+
+# ---------------------------------------------------------------------------------------- end to end
+@pytest.mark.parametrize("wtype", BLOCK_TYPES)
+def test_quantize_then_gemm_end_to_end(wtype):
+    M, N, K = 150, 260, 1024
+    pb = synth.make_problem(wtype, M, N, K, seed=41 + wtype)
+    xq = api.quantize_q8_1(_dev(pb.x))
+    out = api.gemm(wtype, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    q, d, s = oracle.quantize_q8_1(pb.x)
+    assert _rel_err(out, oracle.gemm(wtype, pb.W, q, d, s, N)) <= TOL
+
+
+# ---------------------------------------------------------------------------------------- MoE
+@pytest.mark.parametrize("wtype", [synth.IQ1_M, synth.Q4_K, synth.Q8_0])
+@pytest.mark.parametrize("M,E,slots,N,K", [(24, 6, 3, 130, 256), (300, 16, 4, 256, 512)])
+def test_gemm_id_matches_oracle(wtype, M, E, slots, N, K):
+    pb = synth.make_problem(wtype, M, N, K, seed=51 + M + wtype, experts=E, slots=slots)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm_id(wtype, _dev(pb.W.reshape(-1)), E, xq, _dev(pb.ids), M, N, K).cpu().numpy()
+    ref = oracle.gemm_id(wtype, pb.W, E, q, d, s, pb.ids, N)
+    for t in range(M):
+        for j in range(slots):
+            assert _rel_err(out[t, j], ref[t, j]) <= TOL, (t, j)
+
+
+def test_gemm_id_skewed_routing():
+    # every token routes slot 0 to expert 0: one expert receives M rows (several token tiles)
+    M, E, slots, N, K = 300, 8, 2, 130, 256
+    pb = synth.make_problem(synth.IQ1_M, M, N, K, seed=61, experts=E, slots=slots)
+    pb.ids[:, 0] = 0
+    pb.ids[:, 1] = 1 + np.arange(M) % (E - 1)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm_id(synth.IQ1_M, _dev(pb.W.reshape(-1)), E, xq, _dev(pb.ids), M, N, K).cpu().numpy()
+    ref = oracle.gemm_id(synth.IQ1_M, pb.W, E, q, d, s, pb.ids, N)
+    assert _rel_err(out, ref) <= TOL
+
+
+def test_gemm_id_out_of_range_ids_flagged_and_skipped():
+    M, E, slots, N, K = 8, 4, 2, 128, 256
+    pb = synth.make_problem(synth.Q4_0, M, N, K, seed=71, experts=E, slots=slots)
+    ids = pb.ids.copy()
+    ids[3, 1] = E + 5
+    q, d, s, xq = _oracle_acts(pb)
+    out = torch.full((M, slots, N), 7.0, device=DEV)
+    api.gemm_id(synth.Q4_0, _dev(pb.W.reshape(-1)), E, xq, _dev(ids), M, N, K, out=out)
+    bits = api.read_device_errors()
+    assert bits & api.DEVERR_EXPERT_ID
+    assert torch.all(out[3, 1] == 7.0)
+    ids_ok = ids.copy()
+    ids_ok[3, 1] = ids[3, 0]
+    ref = oracle.gemm_id(synth.Q4_0, pb.W, E, q, d, s, np.where(ids < E, ids, 0).astype(np.int32), N)
+    o = out.cpu().numpy()
+    for t in range(M):
+        for j in range(slots):
+            if (t, j) != (3, 1):
+                assert _rel_err(o[t, j], ref[t, j]) <= TOL
+
+
+# ---------------------------------------------------------------------------------------- degenerate sizes
+def test_empty_inputs_are_noops():
+    W = torch.zeros(1024, dtype=torch.uint8, device=DEV)
+    xq = torch.zeros(1024, dtype=torch.uint8, device=DEV)
+    out = torch.zeros(16, device=DEV)
+    assert api.load().mmq_gemm(synth.Q4_0, W.data_ptr(), xq.data_ptr(), out.data_ptr(), 0, 5, 256, None) == 0
+    assert api.load().mmq_gemm(synth.Q4_0, W.data_ptr(), xq.data_ptr(), out.data_ptr(), 5, 0, 256, None) == 0
+    assert api.load().mmq_quantize_q8_1(out.data_ptr(), 0, 32, xq.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
