@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the MMQ hot path on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole path over one batch: q8_1 activation quantization followed by the
+block-quantized GEMM (for W8A8 the GEMM alone; for MoE quantization, routing and the grouped GEMM).
+The default workload is the 7B-shaped Q4_0 prefill GEMM (M=2048 tokens, N=4096, K=4096) on seeded
+synthetic data.  Timing: W warm-up steps, then K timed steps, each bracketed by CUDA events on the
+launching stream, with a 256 MiB write between steps so that L2 (129 MB) starts cold; device time is
+the sum of step durations, max over ranks.  `e2e` repeats the step through the C-ABI with the
+activations copied from pinned host memory and the output copied back inside the timed region.
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on a bounded sample of the same
+workload on the host cores and prints the same line with "impl": "reference".
+Multi-GPU (torchrun): every rank runs an independent replica of the workload; value is the sum of
+the units all ranks processed over the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_quantized_int8_q8_gb300 import synth  # noqa: E402
+
+METRIC = "effective int8 TOPS (2MNK/t) & prefill tok/s per type/shape; % of GB300 int8 peak"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------------------------------ helpers
+def workload_ops(name: str) -> tuple[float, int]:
+    """(2*M*N*K of the whole step, tokens per step); MoE counts every (token, slot) row."""
+    w = synth.WORKLOADS[name]
+    rows = w["M"] * w.get("slots", 1)
+    return 2.0 * rows * w["N"] * w["K"], w["M"]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_int8_q8_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            self.path = os.path.join("/tmp", f"mmq_clocks_{os.getpid()}.csv")
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "20", "-i", self.gpu_id], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        """Wall-clock window (time.time()) of the timed region; samples outside it are ignored."""
+        self.window = (t0, t1)
+
+    def stop(self):
+        import datetime
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                cols = [c.strip() for c in line.split(",")]
+                if len(cols) < 9:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(cols[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    w = getattr(self, "window", None)
+                    if w and not (w[0] - 0.03 <= ts <= w[1] + 0.03):
+                        continue
+                    sm.append(float(cols[1].split()[0]))
+                    mx.append(float(cols[2].split()[0]))
+                    pw.append(float(cols[3].split()[0]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, cols[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.remove(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch, dev_index: int) -> str:
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        uuid = getattr(p, "uuid", None)
+        if uuid:
+            u = str(uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        bus = getattr(p, "pci_bus_id", None)
+        dom = getattr(p, "pci_domain_id", 0)
+        devn = getattr(p, "pci_device_id", 0)
+        if bus is not None:
+            return f"{dom:08x}:{bus:02x}:{devn:02x}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev_index]
+    return str(dev_index)
+
+
+# ------------------------------------------------------------------------------------------ CPU oracle
+def oracle_step_sample(pb, rows):
+    """One CPU-oracle pass over a sample of token rows (quantize those rows, then the blockwise GEMM)."""
+    import oracle
+    if pb.wtype == synth.W8A8:
+        return oracle.w8a8(pb.fields.W, pb.fields.ws, pb.X[rows], pb.xs[rows])
+    q, d, s = oracle.quantize_q8_1(pb.x[rows])
+    if pb.ids is not None:
+        return oracle.gemm_id(pb.wtype, pb.W, pb.experts, q, d, s, pb.ids[rows], pb.N)
+    return oracle.gemm(pb.wtype, pb.W, q, d, s, pb.N)
+
+
+def cpu_rows_for(pb, target_s: float):
+    """Token rows of a sample that takes about target_s seconds on the host cores."""
+    # fit t(rows) = fixed (weight decode) + rows * per_row from two probe sizes
+    sizes = [min(4, pb.M), min(16, pb.M)]
+    ts = []
+    for n in sizes:
+        t = time.perf_counter()
+        oracle_step_sample(pb, list(range(n)))
+        ts.append(time.perf_counter() - t)
+    per_row = max((ts[1] - ts[0]) / max(sizes[1] - sizes[0], 1), 1e-9) if sizes[1] > sizes[0] else ts[0]
+    fixed = max(ts[0] - per_row * sizes[0], 0.0)
+    n = int(max(1, min(pb.M, (target_s - fixed) / per_row)))
+    return list(range(n))
+
+
+def cpu_baseline(pb, name, target_s=10.0):
+    import oracle
+    rows = cpu_rows_for(pb, target_s)
+    t = time.perf_counter()
+    oracle_step_sample(pb, rows)
+    dt = time.perf_counter() - t
+    ops_full, tokens = workload_ops(name)
+    ops = ops_full * len(rows) / pb.M
+    return {"value": ops / dt / 1e12, "unit": "TOPS", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {pb.M} token rows of {name}, quantize + blockwise GEMM, "
+                      f"{dt:.1f} s on the host cores", "tok_per_s": len(rows) / dt}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    pb = synth.workload(args.workload)
+    ops_full, tokens = workload_ops(args.workload)
+    rows = cpu_rows_for(pb, args.ref_step_s)
+    for _ in range(args.warmup):
+        oracle_step_sample(pb, rows)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle_step_sample(pb, rows)
+        times.append(time.perf_counter() - t)
+    ops = ops_full * len(rows) / pb.M
+    total = sum(times)
+    value = ops * args.steps / total / 1e12
+    import oracle
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 x q8_1 (CPU oracle)",
+            "data": "synthetic", "config": workload_config(args.workload),
+            "tok_per_s": len(rows) * args.steps / total,
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"{len(rows)} of {pb.M} token rows per step (quantize + blockwise GEMM)"},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def rescale_ceiling(wt, ops, ffma_tflops):
+    """FP32-pipe ceiling of the per-block rescale: each 32-k element-block (64 ops of the contraction)
+    costs two FP32 instructions (scale product, fused multiply-add), three for Q4_K (min term)."""
+    if not ffma_tflops or wt == synth.W8A8:
+        return None
+    instr = 3 if wt == synth.Q4_K else 2
+    fp32_instr_per_s = ffma_tflops * 1e12 / 2
+    return {"ffma_tflops": ffma_tflops, "fp32_instr_per_element_block": instr, "element_blocks": ops / 64,
+            "ceiling_tops": fp32_instr_per_s / instr * 64 / 1e12}
+
+
+def workload_config(name):
+    w = synth.WORKLOADS[name]
+    cfg = {"workload": name, "wtype": synth.TYPE_NAMES[w["wtype"]].upper(), "M_tokens": w["M"], "N": w["N"],
+           "K": w["K"], "seed": w["seed"], "l2": "flushed between timed steps (256 MiB write)"}
+    if "experts" in w:
+        cfg.update(experts=w["experts"], slots=w["slots"])
+    return cfg
+
+
+# ------------------------------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mmq", "reference"], default="mmq")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="q4_0_7b")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
+    ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from block_quantized_int8_q8_gb300 import _build, api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    api.load()
+
+    name = args.workload
+    pb = synth.workload(name)
+    wt = pb.wtype
+    M, N, K = pb.M, pb.N, pb.K
+    ops, tokens = workload_ops(name)
+    W = torch.from_numpy(pb.W.reshape(-1)).to(dev)
+    stream = torch.cuda.current_stream()
+    is_moe = pb.ids is not None
+    if wt == synth.W8A8:
+        x = torch.from_numpy(synth.pack_w8a8_acts(pb.X, pb.xs)).to(dev)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        launches_per_step = 1
+    else:
+        x = torch.from_numpy(pb.x).to(dev)
+        xq = torch.empty(api.q8_1_bytes(M, K), dtype=torch.uint8, device=dev)
+        if is_moe:
+            ids = torch.from_numpy(pb.ids).to(dev)
+            out = torch.empty((M, pb.ids.shape[1], N), dtype=torch.float32, device=dev)
+            ws = torch.empty(api.gemm_id_workspace_bytes(M, pb.ids.shape[1], pb.experts), dtype=torch.uint8,
+                             device=dev)
+            launches_per_step = 6           # quantize, 4 routing kernels, grouped GEMM
+        else:
+            out = torch.empty((M, N), dtype=torch.float32, device=dev)
+            launches_per_step = 2           # quantize, GEMM
+
+    def gemm_call():
+        if wt == synth.W8A8:
+            api.gemm(wt, W, x, M, N, K, out=out)
+        elif is_moe:
+            api.gemm_id(wt, W, pb.experts, xq, ids, M, N, K, out=out, workspace=ws)
+        else:
+            api.gemm(wt, W, xq, M, N, K, out=out)
+
+    def quant_call():
+        if wt != synth.W8A8:
+            api.quantize_q8_1(x, out=xq)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        quant_call()
+        gemm_call()
+    torch.cuda.synchronize()
+    assert api.read_device_errors() == 0
+
+    # ---------------------------------------------------------------- timed region
+    K_steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_steps)]
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    sampler.start()
+    time.sleep(0.15)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    tw0 = time.time()
+    for i in range(K_steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        quant_call()
+        ev[i][1].record(stream)
+        gemm_call()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    sampler.mark(tw0, time.time())
+    clocks = sampler.stop()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K_steps)]
+    gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K_steps)]
+    quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K_steps)]
+    dev_total = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([dev_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_total = float(t.item())
+    errs = api.read_device_errors()
+
+    # ---------------------------------------------------------------- end to end through the C ABI
+    e2e = None
+    if args.e2e_steps > 0:
+        if wt == synth.W8A8:
+            host_in = torch.from_numpy(synth.pack_w8a8_acts(pb.X, pb.xs)).pin_memory()
+        else:
+            host_in = torch.from_numpy(pb.x).pin_memory()
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):
+            x.copy_(host_in, non_blocking=True)
+            quant_call()
+            gemm_call()
+            host_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            x.copy_(host_in, non_blocking=True)
+            quant_call()
+            gemm_call()
+            host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_s = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": ops * world * args.e2e_steps / e2e_s / 1e12, "unit": "TOPS",
+               "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
+               "steps": args.e2e_steps, "note": "weights resident in HBM; activations in, outputs out"}
+
+    # ---------------------------------------------------------------- roofline and peaks
+    peaks, peak_src = measured_peaks()
+    gemm_avg = statistics.mean(gemm_ms) / 1e3
+    achieved = ops / gemm_avg / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "kernel": "mmq_gemm_kernel", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(name),
+                "peak_source": f"{peak_src} dense bf16 burst (fp16 operands, same nominal rate)",
+                "flops_per_launch": ops}
+    int8_peak = ffma = None
+    try:
+        import ctypes
+        plib = ctypes.CDLL(_build.PEAKS_LIB)
+        plib.mmq_peak_int8_mma_sync.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.c_int, ctypes.c_void_p]
+        plib.mmq_peak_ffma.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.c_int, ctypes.c_void_p]
+        v = ctypes.c_double(0)
+        if plib.mmq_peak_int8_mma_sync(ctypes.byref(v), 4096, ctypes.c_void_p(stream.cuda_stream)) == 0:
+            int8_peak = v.value
+        if plib.mmq_peak_ffma(ctypes.byref(v), 4096, ctypes.c_void_p(stream.cuda_stream)) == 0:
+            ffma = v.value
+    except OSError:
+        pass
+
+    value = ops * world * K_steps / dev_total / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": K_steps,
+            "warmup": args.warmup, "ms_per_step": dev_total / K_steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "s8 x s8 -> exact block dot (fp16 tensor cores, f32 accumulate), f32 rescale",
+            "data": "synthetic", "config": workload_config(name),
+            "tok_per_s": tokens * world * K_steps / dev_total,
+            "pct_int8_peak": (100.0 * value / world / int8_peak) if int8_peak else None,
+            "int8_peak_tops": int8_peak,
+            "int8_peak_source": "measured live: mma.sync.m16n8k32.s8, the only int8 tensor path on sm_103a",
+            "gemm_ms": statistics.mean(gemm_ms), "quantize_ms": statistics.mean(quant_ms),
+            "gemm_only_tops": ops / gemm_avg / 1e12,
+            "roofline": roofline,
+            "rescale_ceiling": rescale_ceiling(wt, ops, ffma),
+            "e2e": e2e, "gpu_launches": launches_per_step * K_steps, "clocks": clocks,
+            "wall_s": wall, "device_errors": errs}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(pb, name, args.cpu_baseline_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

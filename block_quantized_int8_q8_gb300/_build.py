@@ -12,6 +12,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libmmq_gb300.so")
+PEAKS_LIB = os.path.join(LIBDIR, "libmmq_peaks.so")
+PEAKS_SRC = os.path.join(PKG, "probe", "peaks.cu")
 OBJDIR = os.path.join(ROOT, "_build", "obj")
 
 NVCC = os.environ.get("NVCC", "nvcc")
@@ -29,10 +31,13 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
-        return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    for lib, deps in ((LIB, _deps()), (PEAKS_LIB, [PEAKS_SRC, os.path.join(ROOT, "include", "mmq_peaks.h")])):
+        if not os.path.exists(lib):
+            return False
+        t = os.path.getmtime(lib)
+        if any(os.path.getmtime(d) > t for d in deps):
+            return False
+    return True
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -52,7 +57,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return obj
 
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, sources()))
+        objs = list(ex.map(compile_one, sources() + [PEAKS_SRC]))
+    peaks_obj = objs.pop()
+    tmp = PEAKS_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, peaks_obj, "-lcudart"], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stderr}")
+    os.replace(tmp, PEAKS_LIB)
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
