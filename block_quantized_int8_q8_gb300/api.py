@@ -20,7 +20,8 @@ DEVERR_TIMEOUT, DEVERR_EXPERT_ID, DEVERR_DUP_EXPERT = 1, 2, 4
 #: every symbol include/mmq.h declares
 EXPORTS = ("mmq_status_string", "mmq_last_cuda_error", "mmq_q8_1_bytes", "mmq_weight_bytes", "mmq_w8a8_act_bytes", "mmq_quantize_q8_1",
            "mmq_gemm", "mmq_gemm_id_workspace_bytes", "mmq_gemm_id", "mmq_gemm_debug_partials",
-           "mmq_read_device_errors")
+           "mmq_read_device_errors", "mmq_gemm_id_noalloc")
+NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
 
@@ -63,6 +64,8 @@ def load():
     lib.mmq_gemm_id.restype = I
     lib.mmq_gemm_debug_partials.argtypes = [I, P, P, P, I64, I64, I64, P]
     lib.mmq_gemm_debug_partials.restype = I
+    lib.mmq_gemm_id_noalloc.argtypes = [I, P, I, P, P, I, P, I64, I64, I64, P]
+    lib.mmq_gemm_id_noalloc.restype = I
     lib.mmq_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), P]
     lib.mmq_read_device_errors.restype = I
     _lib = lib
@@ -162,6 +165,18 @@ def gemm_id(wtype: int, W: torch.Tensor, n_experts: int, Xq: torch.Tensor, ids: 
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=W.device)
     _check(load().mmq_gemm_id(wtype, _ptr(W), n_experts, _ptr(Xq), _ptr(ids), slots, _ptr(out), M, N, K,
                               _ptr(workspace), workspace.numel(), _stream(stream)), "mmq_gemm_id")
+    return out
+
+
+def gemm_id_noalloc(wtype: int, W: torch.Tensor, n_experts: int, Xq: torch.Tensor, ids: torch.Tensor, M: int,
+                    N: int, K: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """MoE MUL_MAT_ID without a workspace (mmq_gemm_id_noalloc): the routing lists live in the
+    library's static device scratch array, for callers that cannot allocate device memory."""
+    slots = ids.shape[1]
+    if out is None:
+        out = torch.empty((M, slots, N), dtype=torch.float32, device=W.device)
+    _check(load().mmq_gemm_id_noalloc(wtype, _ptr(W), n_experts, _ptr(Xq), _ptr(ids), slots, _ptr(out), M, N, K,
+                                      _stream(stream)), "mmq_gemm_id_noalloc")
     return out
 
 

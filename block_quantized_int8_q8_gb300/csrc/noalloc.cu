@@ -1,0 +1,121 @@
+// noalloc.cu -- mmq_gemm_id_noalloc: the MoE product for callers that cannot allocate device memory.
+//
+// Who needs this: code that runs where cudaMalloc is unavailable or forbidden -- inside a
+// stream-capture region that must not allocate, under an allocator that owns all device memory
+// (a framework's caching pool, a serving engine with a fixed memory budget), or in a plugin that is
+// handed only its input and output buffers.  mmq_gemm_id needs a caller-supplied workspace for its
+// routing lists; this variant keeps that workspace in a file-scope device array instead.
+//
+// The scratch array is MMQ_NOALLOC_SCRATCH_BYTES (1 MiB) of static device memory: every GPU that
+// loads the library holds it until the process exits.  All calls share it and it keeps the last
+// call's contents; the routing kernels rewrite every entry they later read (the per-expert counts
+// are cleared at the start of each call), so nothing has to be zero on entry.  Two calls whose
+// kernels overlap on the GPU (different streams, no ordering between them) race on the array.
+#include <cstdint>
+#include <mutex>
+#include <cuda_runtime.h>
+#include "../../include/mmq.h"
+#include "gemm.cuh"
+#include "internal.h"
+
+using namespace mmq;
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MMQ_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array for the current device.  The symbol name is a host-side
+// stand-in, so the address must come from cudaGetSymbolAddress, once per device, with that device
+// current.  This runs on the first call on each device.
+cudaError_t scratch_for_current_device(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+long long row_bytes(mmq_type t, long long K) {
+    switch (t) {
+        case MMQ_Q8_0: return K / 32 * 34;
+        case MMQ_Q4_0: return K / 32 * 18;
+        case MMQ_Q4_K: return K / 256 * 144;
+        case MMQ_IQ1_M: return K / 256 * 76;
+        default: return -1;
+    }
+}
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_experts, const void* Xq,
+                                          const int32_t* expert_ids, int n_slots, float* out, int64_t M,
+                                          int64_t N, int64_t K, mmq_stream_t stream) {
+    if (wtype < MMQ_Q8_0 || wtype > MMQ_IQ1_M) return wtype == MMQ_W8A8 ? MMQ_ERR_UNSUPPORTED : MMQ_ERR_INVALID_ARG;
+    if (n_experts <= 0 || n_slots <= 0) return MMQ_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return MMQ_ERR_SHAPE;
+    if (M * K >= (1ll << 31) || N * K >= (1ll << 31) || M * n_slots >= (1ll << 31)) return MMQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return MMQ_OK;
+    if (!W || !Xq || !expert_ids || !out) return MMQ_ERR_INVALID_ARG;
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al(W) || !al(Xq) || !al(out) || !al(expert_ids)) return MMQ_ERR_ALIGN;
+
+    // carve the routing lists out of the scratch array (same layout as the mmq_gemm_id workspace)
+    const long long rows = M * n_slots;
+    const int max_work = (int)((rows + BN - 1) / BN + n_experts);
+    const size_t counts = 0, offsets = counts + round256(4ull * n_experts), cursor = offsets + round256(4ull * n_experts);
+    const size_t nwork = cursor + round256(4ull * n_experts), work = nwork + round256(4);
+    const size_t rowlist = work + round256(12ull * max_work), total = rowlist + round256(4ull * rows);
+    if (total > MMQ_NOALLOC_SCRATCH_BYTES) return MMQ_ERR_WORKSPACE;   // problem too large for the array
+
+    void* base = nullptr;
+    if (scratch_for_current_device(&base) != cudaSuccess) return MMQ_ERR_CUDA;
+    uint8_t* sb = static_cast<uint8_t*>(base);
+    RouteWorkspace ws;
+    ws.counts = reinterpret_cast<int*>(sb + counts);
+    ws.offsets = reinterpret_cast<int*>(sb + offsets);
+    ws.cursor = reinterpret_cast<int*>(sb + cursor);
+    ws.nwork = reinterpret_cast<int*>(sb + nwork);
+    ws.work = reinterpret_cast<int*>(sb + work);
+    ws.rowlist = reinterpret_cast<int*>(sb + rowlist);
+    ws.max_work = max_work;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s) != cudaSuccess) return MMQ_ERR_CUDA;
+
+    GemmParams p{};
+    p.W = static_cast<const uint8_t*>(W);
+    p.xq = static_cast<const int8_t*>(Xq);
+    p.xds = reinterpret_cast<const float4*>(static_cast<const uint8_t*>(Xq) + M * K);
+    p.out = out;
+    p.w_row_bytes = row_bytes(wtype, K);
+    p.w_expert_bytes = p.w_row_bytes * N;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.rowlist = ws.rowlist;
+    p.work = ws.work;
+    p.nwork = ws.nwork;
+    p.slots = n_slots;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (wtype) {
+        case MMQ_Q8_0: e = run_gemm_q8_0(p, MODE_PROD, true, max_work, s); break;
+        case MMQ_Q4_0: e = run_gemm_q4_0(p, MODE_PROD, true, max_work, s); break;
+        case MMQ_Q4_K: e = run_gemm_q4_k(p, MODE_PROD, true, max_work, s); break;
+        case MMQ_IQ1_M: e = run_gemm_iq1_m(p, MODE_PROD, true, max_work, s); break;
+        default: break;
+    }
+    return e == cudaSuccess ? MMQ_OK : MMQ_ERR_CUDA;
+}

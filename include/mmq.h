@@ -141,6 +141,25 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
                        mmq_stream_t stream);
 
 /*
+ * mmq_gemm_id_noalloc -- mmq_gemm_id for callers that cannot allocate device memory.  The pages have
+ * no counterpart: it exists for integrations where cudaMalloc is not available or not allowed (code
+ * inside a memory-budgeted serving engine or a framework's caching allocator, plugins that are given
+ * only their input and output buffers), which cannot provide mmq_gemm_id's workspace.
+ * Arguments and results are those of mmq_gemm_id without the workspace.  The routing lists live in a
+ * file-scope device array of MMQ_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the
+ * library until the process exits; the call itself allocates nothing.  Problems whose routing lists
+ * need more than that (mmq_gemm_id_workspace_bytes(M, n_slots, n_experts) > MMQ_NOALLOC_SCRATCH_BYTES)
+ * are rejected with MMQ_ERR_WORKSPACE.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  All calls share the array: calls whose kernels may overlap on the GPU (unordered streams)
+ * race and must be serialised by the caller.
+ */
+#define MMQ_NOALLOC_SCRATCH_BYTES (1u << 20)
+mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_experts, const void* Xq,
+                               const int32_t* expert_ids, int n_slots, float* out,
+                               int64_t M, int64_t N, int64_t K, mmq_stream_t stream);
+
+/*
  * mmq_gemm_debug_partials -- debug mode: the exact per-group integer dots the tensor-core path
  * computes ("08 · R1", §2.1: the in-block int8 dot is exact in int32).
  * partials : int32 [M][N][K/G], G = 16 for IQ1_M (per-16 halves, values 8g±1), else 32; for W8A8 the
