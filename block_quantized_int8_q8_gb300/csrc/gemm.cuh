@@ -39,7 +39,8 @@ enum Mode { MODE_PROD = 0, MODE_DEBUG = 1 };
 constexpr int BM = 128;             // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;             // tokens per tile (MMA N)
 constexpr int BK = 64;              // k per pipeline stage: one 128-byte swizzle row of fp16
-constexpr int STAGES = 4;           // smem pipeline depth
+constexpr int STAGES = 4;           // smem operand pipeline depth
+constexpr int SC_STAGES = 8;        // scale ring depth (released by the epilogue, so deeper)
 constexpr int NACC = 4;             // TMEM accumulators (BN columns each)
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_PROD_WARPS = 4;
@@ -58,10 +59,10 @@ struct SmemLayout {
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
     static constexpr int sc_off = b_off + STAGES * B_STAGE_BYTES;
-    static constexpr int orow_off = sc_off + STAGES * SC_STAGE_FLOATS * 4;
+    static constexpr int orow_off = sc_off + SC_STAGES * SC_STAGE_FLOATS * 4;
     static constexpr int trow_off = orow_off + BN * 4;
     static constexpr int bar_off = trow_off + BN * 4;           // 8-byte aligned
-    static constexpr int n_bars = 4 * STAGES + 2 * NACC + 1;
+    static constexpr int n_bars = 2 * STAGES + 2 * SC_STAGES + 2 * NACC + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;       // tmem slot, abort flag
     static constexpr int total = misc_off + 16;
     static constexpr int alloc = total + 1024;                  // slack for 1024-byte alignment
@@ -238,8 +239,10 @@ struct KTraits {
 template <int WT, int MODE, bool MOE>
 __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams p) {
     using T = KTraits<WT, MODE>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // align by pointer arithmetic on the __shared__ array so that the compiler keeps the address space
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t smem_s = smem_u32(smem);                   // shared-window address of the tile base
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ---- tile coordinates
@@ -254,27 +257,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
     }
     const uint8_t* Wbase = p.W + (long long)expert * p.w_expert_bytes;
 
-    float* sc_base = reinterpret_cast<float*>(smem + SmemLayout::sc_off);
     int* orow = reinterpret_cast<int*>(smem + SmemLayout::orow_off);
     int* trow = reinterpret_cast<int*>(smem + SmemLayout::trow_off);
     const uint32_t bar0 = smem_u32(smem + SmemLayout::bar_off);
     auto bar_full = [&](int i) { return bar0 + 8u * i; };
     auto bar_empty = [&](int i) { return bar0 + 8u * (STAGES + i); };
     auto bar_sfull = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
-    auto bar_sfree = [&](int i) { return bar0 + 8u * (3 * STAGES + i); };
-    auto bar_accf = [&](int i) { return bar0 + 8u * (4 * STAGES + i); };
-    auto bar_acce = [&](int i) { return bar0 + 8u * (4 * STAGES + NACC + i); };
-    const uint32_t bar_done = bar0 + 8u * (4 * STAGES + 2 * NACC);
+    auto bar_sfree = [&](int i) { return bar0 + 8u * (2 * STAGES + SC_STAGES + i); };
+    auto bar_accf = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 * SC_STAGES + i); };
+    auto bar_acce = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 * SC_STAGES + NACC + i); };
+    const uint32_t bar_done = bar0 + 8u * (2 * STAGES + 2 * SC_STAGES + 2 * NACC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
 
     // ---- setup: barriers, TMEM, row maps
     if (warp == MMA_WARP) {
         if (lane == 0) {
+            // one arrival per producer warp (an elected lane after the warp's stores are fenced):
+            // per-thread arrivals on one barrier word serialise and throttle the whole pipeline
             for (int i = 0; i < STAGES; i++) {
-                mbar_init(bar_full(i), NUM_PROD_WARPS * 32);
+                mbar_init(bar_full(i), NUM_PROD_WARPS);
                 mbar_init(bar_empty(i), 1);
-                mbar_init(bar_sfull(i), NUM_PROD_WARPS * 32);
+            }
+            for (int i = 0; i < SC_STAGES; i++) {
+                mbar_init(bar_sfull(i), NUM_PROD_WARPS);
                 mbar_init(bar_sfree(i), NUM_EPI_WARPS);
             }
             for (int i = 0; i < NACC; i++) {
@@ -352,8 +358,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
         auto produce = [&](RawSet& rs, int s) {
             const int slot = s % STAGES;
             const uint32_t par = ((s / STAGES) & 1) ^ 1;
+            const int sslot = s % SC_STAGES;
+            if constexpr (T::kScaleRing) mbar_wait(bar_sfree(sslot), ((s / SC_STAGES) & 1) ^ 1, abort_flag);
             mbar_wait(bar_empty(slot), par, abort_flag);
-            if constexpr (T::kScaleRing) mbar_wait(bar_sfree(slot), par, abort_flag);
             const uint32_t at = a_smem + slot * A_STAGE_BYTES;
             const uint32_t bt = b_smem + slot * B_STAGE_BYTES;
             {
@@ -365,15 +372,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                 for (int c = 0; c < 8; c++)
                     st_shared_v4(at + sw128_off(r, c), ha[4 * c], ha[4 * c + 1], ha[4 * c + 2], ha[4 * c + 3]);
                 if constexpr (T::kScaleRing) {
-                    float* sc = sc_base + slot * SC_STAGE_FLOATS;
-                    sc[0 * BM + r] = wsc[0];
-                    sc[1 * BM + r] = wsc[1];
-                    sc[2 * BM + r] = wmn[0];
-                    sc[3 * BM + r] = wmn[1];
-                    sc[4 * BM + r] = rs.ds.x;                 // xd, block 0
-                    sc[4 * BM + BN + r] = rs.ds.z;            // xd, block 1
-                    sc[4 * BM + 2 * BN + r] = rs.ds.y;        // xs, block 0
-                    sc[4 * BM + 3 * BN + r] = rs.ds.w;        // xs, block 1
+                    const uint32_t sc = smem_s + SmemLayout::sc_off + sslot * SC_STAGE_FLOATS * 4 + 4 * r;
+                    st_shared_f32(sc + 4 * (0 * BM), wsc[0]);
+                    st_shared_f32(sc + 4 * (1 * BM), wsc[1]);
+                    st_shared_f32(sc + 4 * (2 * BM), wmn[0]);
+                    st_shared_f32(sc + 4 * (3 * BM), wmn[1]);
+                    st_shared_f32(sc + 4 * (4 * BM), rs.ds.x);              // xd, block 0
+                    st_shared_f32(sc + 4 * (4 * BM + BN), rs.ds.z);         // xd, block 1
+                    st_shared_f32(sc + 4 * (4 * BM + 2 * BN), rs.ds.y);     // xs, block 0
+                    st_shared_f32(sc + 4 * (4 * BM + 3 * BN), rs.ds.w);     // xs, block 1
                 }
             }
 #pragma unroll
@@ -386,9 +393,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                 st_shared_v4(bt + sw128_off(r, 2 * i), hb[0], hb[1], hb[2], hb[3]);
                 st_shared_v4(bt + sw128_off(r, 2 * i + 1), hb[4], hb[5], hb[6], hb[7]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar_full(slot));
-            if constexpr (T::kScaleRing) mbar_arrive(bar_sfull(slot));
+            fence_proxy_async_smem();       // this thread's tile stores -> visible to the tensor core
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) {
+                mbar_arrive(bar_full(slot));
+                if constexpr (T::kScaleRing) mbar_arrive(bar_sfull(sslot));
+            }
         };
 
         RawSet set0, set1;
@@ -442,10 +452,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
         const int n = n0 + r;
         const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + 64 * ch;
 
-        float acc[(MODE == MODE_PROD && !T::kIsW8) ? 64 : 1];
+        uint64_t acc2[(MODE == MODE_PROD && !T::kIsW8) ? 32 : 1];   // packed f32 pairs: columns 2t, 2t+1
         int32_t iacc[T::kIsW8 ? 64 : 1];
 #pragma unroll
-        for (int j = 0; j < (int)(sizeof(acc) / sizeof(float)); j++) acc[j] = 0.f;
+        for (int j = 0; j < (int)(sizeof(acc2) / sizeof(uint64_t)); j++) acc2[j] = 0ull;
         if constexpr (T::kIsW8) {
 #pragma unroll
             for (int j = 0; j < 64; j++) iacc[j] = 0;
@@ -455,25 +465,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
             const int buf = g % NACC;
             mbar_wait(bar_accf(buf), (g / NACC) & 1, abort_flag);
             tc_fence_after();
-            const float* sc = nullptr;
+            uint32_t sc = 0;
             float rs = 0.f, mn = 0.f;
             int slot = 0, i = 0;
             if constexpr (T::kScaleRing) {
                 const int s = g >> 1;
                 i = g & 1;
-                slot = s % STAGES;
-                if (i == 0) mbar_wait(bar_sfull(slot), (s / STAGES) & 1, abort_flag);
-                sc = sc_base + slot * SC_STAGE_FLOATS;
-                rs = sc[i * BM + r];
-                if constexpr (WT == WT_Q4_K) mn = sc[2 * BM + i * BM + r];
+                slot = s % SC_STAGES;
+                if (i == 0) mbar_wait(bar_sfull(slot), (s / SC_STAGES) & 1, abort_flag);
+                sc = smem_s + SmemLayout::sc_off + slot * SC_STAGE_FLOATS * 4;
+                rs = ld_shared_f32(sc + 4 * (i * BM + r));
+                if constexpr (WT == WT_Q4_K) mn = ld_shared_f32(sc + 4 * (2 * BM + i * BM + r));
             }
-            // two halves of 32 columns: load, then rescale, so only 32 partials are live at a time
+            const uint64_t rs2 = f2_pack(rs, rs);
+            const uint64_t nmn2 = f2_pack(-mn, -mn);
+            // four quarters of 16 columns; each quarter's column scales are requested before its
+            // TMEM load so that the two latencies overlap
 #pragma unroll
-            for (int hh = 0; hh < 2; hh++) {
-                uint32_t v[32];
-                tmem_ld32(tbase + buf * BN + 32 * hh, v);
+            for (int qq = 0; qq < 4; qq++) {
+                float4 c[4], cs[4];
+                if constexpr (T::kScaleRing) {
+                    const uint32_t xd = sc + 4 * (4 * BM + i * BN + 64 * ch + 16 * qq);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; q4++) c[q4] = ld_shared_f4(xd + 16 * q4);
+                    if constexpr (WT == WT_Q4_K) {
+                        const uint32_t xs = sc + 4 * (4 * BM + 2 * BN + i * BN + 64 * ch + 16 * qq);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; q4++) cs[q4] = ld_shared_f4(xs + 16 * q4);
+                    }
+                }
+                uint32_t v[16];
+                tmem_ld16(tbase + buf * BN + 16 * qq, v);
                 tmem_ld_wait();
-                if (hh == 1) {
+                if (qq == 3) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acce(buf));
@@ -481,8 +505,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                 if constexpr (MODE == MODE_DEBUG) {
                     if (n < p.N) {
 #pragma unroll
-                        for (int j = 0; j < 32; j++) {
-                            const int col = 64 * ch + 32 * hh + j;
+                        for (int j = 0; j < 16; j++) {
+                            const int col = 64 * ch + 16 * qq + j;
                             if (col < mcount)
                                 p.partials[((long long)(m0 + col) * p.N + n) * ngroups + g] =
                                     __float2int_rn(__uint_as_float(v[j]));
@@ -490,26 +514,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                     }
                 } else if constexpr (T::kIsW8) {
 #pragma unroll
-                    for (int j = 0; j < 32; j++) iacc[32 * hh + j] += __float2int_rn(__uint_as_float(v[j]));
+                    for (int j = 0; j < 16; j++) iacc[16 * qq + j] += __float2int_rn(__uint_as_float(v[j]));
                 } else {
-                    const float* xd = sc + 4 * BM + i * BN + 64 * ch + 32 * hh;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 c = *reinterpret_cast<const float4*>(xd + j);
-                        acc[32 * hh + j + 0] = fmaf(__uint_as_float(v[j + 0]), rs * c.x, acc[32 * hh + j + 0]);
-                        acc[32 * hh + j + 1] = fmaf(__uint_as_float(v[j + 1]), rs * c.y, acc[32 * hh + j + 1]);
-                        acc[32 * hh + j + 2] = fmaf(__uint_as_float(v[j + 2]), rs * c.z, acc[32 * hh + j + 2]);
-                        acc[32 * hh + j + 3] = fmaf(__uint_as_float(v[j + 3]), rs * c.w, acc[32 * hh + j + 3]);
-                    }
-                    if constexpr (WT == WT_Q4_K) {
-                        const float* xs = sc + 4 * BM + 2 * BN + i * BN + 64 * ch + 32 * hh;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 c = *reinterpret_cast<const float4*>(xs + j);
-                            acc[32 * hh + j + 0] = fmaf(-mn, c.x, acc[32 * hh + j + 0]);
-                            acc[32 * hh + j + 1] = fmaf(-mn, c.y, acc[32 * hh + j + 1]);
-                            acc[32 * hh + j + 2] = fmaf(-mn, c.z, acc[32 * hh + j + 2]);
-                            acc[32 * hh + j + 3] = fmaf(-mn, c.w, acc[32 * hh + j + 3]);
+                    for (int q4 = 0; q4 < 4; q4++) {
+                        const int j = 4 * q4, a = 8 * qq + 2 * q4;
+                        const uint64_t s01 = f2_mul(f2_pack(c[q4].x, c[q4].y), rs2);
+                        const uint64_t s23 = f2_mul(f2_pack(c[q4].z, c[q4].w), rs2);
+                        acc2[a] = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s01, acc2[a]);
+                        acc2[a + 1] = f2_fma(f2_pack(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), s23, acc2[a + 1]);
+                        if constexpr (WT == WT_Q4_K) {
+                            acc2[a] = f2_fma(nmn2, f2_pack(cs[q4].x, cs[q4].y), acc2[a]);
+                            acc2[a + 1] = f2_fma(nmn2, f2_pack(cs[q4].z, cs[q4].w), acc2[a + 1]);
                         }
                     }
                 }
@@ -540,9 +556,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                 } else {
                     float* out = reinterpret_cast<float*>(p.out);
 #pragma unroll
-                    for (int j = 0; j < 64; j++) {
-                        const int orr = orw[j];
-                        if (orr >= 0) out[(long long)orr * p.N + n] = acc[j];
+                    for (int t = 0; t < 32; t++) {
+                        float a0, a1;
+                        f2_unpack(acc2[t], a0, a1);
+                        const int o0 = orw[2 * t], o1 = orw[2 * t + 1];
+                        if (o0 >= 0) out[(long long)o0 * p.N + n] = a0;
+                        if (o1 >= 0) out[(long long)o1 * p.N + n] = a1;
                     }
                 }
             }
