@@ -20,7 +20,7 @@ DEVERR_TIMEOUT, DEVERR_EXPERT_ID, DEVERR_DUP_EXPERT = 1, 2, 4
 #: every symbol include/mmq.h declares
 EXPORTS = ("mmq_status_string", "mmq_last_cuda_error", "mmq_q8_1_bytes", "mmq_weight_bytes", "mmq_w8a8_act_bytes", "mmq_quantize_q8_1",
            "mmq_gemm", "mmq_gemm_id_workspace_bytes", "mmq_gemm_id", "mmq_gemm_debug_partials",
-           "mmq_read_device_errors", "mmq_gemm_id_noalloc")
+           "mmq_read_device_errors", "mmq_gemm_id_noalloc", "mmq_q8_1_prepare")
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
@@ -55,6 +55,8 @@ def load():
     lib.mmq_w8a8_act_bytes.argtypes = [I64, I64]
     lib.mmq_w8a8_act_bytes.restype = SZ
     lib.mmq_quantize_q8_1.argtypes = [P, I64, I64, P, P]
+    lib.mmq_q8_1_prepare.argtypes = [P, I64, I64, P]
+    lib.mmq_q8_1_prepare.restype = I
     lib.mmq_quantize_q8_1.restype = I
     lib.mmq_gemm.argtypes = [I, P, P, P, I64, I64, I64, P]
     lib.mmq_gemm.restype = I
@@ -110,18 +112,43 @@ def gemm_id_workspace_bytes(M: int, slots: int, experts: int) -> int:
     return int(load().mmq_gemm_id_workspace_bytes(M, slots, experts))
 
 
+def q8_1_offsets(M: int, K: int) -> dict:
+    """Byte offsets of the four sections of a q8_1 buffer (layout in include/mmq.h)."""
+    ds = M * K
+    h = (M * K + M * (K // 32) * 8 + 255) // 256 * 256
+    return {"q": 0, "ds": ds, "h": h, "xs3": h + 2 * M * K}
+
+
 def q8_1_views(buf: torch.Tensor, M: int, K: int):
-    """(q int8 [M, K], ds f32 [M, K/32, 2]) views of a q8_1 activation buffer (layout in include/mmq.h)."""
+    """(q int8 [M, K], ds f32 [M, K/32, 2]) views of a q8_1 buffer's block sections."""
+    o = q8_1_offsets(M, K)
     q = buf[: M * K].view(torch.int8).view(M, K)
-    ds = buf[M * K: M * K + M * (K // 32) * 8].view(torch.float32).view(M, K // 32, 2)
+    ds = buf[o["ds"]: o["ds"] + M * (K // 32) * 8].view(torch.float32).view(M, K // 32, 2)
     return q, ds
 
 
-def pack_q8_1(q: torch.Tensor, d: torch.Tensor, s: torch.Tensor) -> torch.Tensor:
-    """Assemble a q8_1 byte buffer from codes [M, K], scales d [M, K/32] and block sums s [M, K/32]."""
+def q8_1_shadow_views(buf: torch.Tensor, M: int, K: int):
+    """(h fp16 [M, K], xs3 bf16 [M, K/32, 8]) views of a q8_1 buffer's derived sections."""
+    o = q8_1_offsets(M, K)
+    h = buf[o["h"]: o["h"] + 2 * M * K].view(torch.float16).view(M, K)
+    xs3 = buf[o["xs3"]: o["xs3"] + M * (K // 32) * 16].view(torch.bfloat16).view(M, K // 32, 8)
+    return h, xs3
+
+
+def q8_1_prepare(buf: torch.Tensor, M: int, K: int, stream=None) -> torch.Tensor:
+    """Fill the derived sections of a q8_1 buffer from its q and ds sections (mmq_q8_1_prepare)."""
+    _check(load().mmq_q8_1_prepare(_ptr(buf), M, K, _stream(stream)), "mmq_q8_1_prepare")
+    return buf
+
+
+def pack_q8_1(q: torch.Tensor, d: torch.Tensor, s: torch.Tensor, device="cuda") -> torch.Tensor:
+    """A complete q8_1 buffer on `device` from codes [M, K], scales d and block sums s [M, K/32]."""
     M, K = q.shape
-    ds = torch.stack([d.float(), s.float()], dim=-1).contiguous()
-    return torch.cat([q.contiguous().view(torch.uint8).reshape(-1), ds.view(torch.uint8).reshape(-1)])
+    buf = torch.zeros(q8_1_bytes(M, K), dtype=torch.uint8, device=device)
+    qv, dsv = q8_1_views(buf, M, K)
+    qv.copy_(q.to(device))
+    dsv.copy_(torch.stack([d.float(), s.float()], dim=-1).to(device))
+    return q8_1_prepare(buf, M, K)
 
 
 # ------------------------------------------------------------------------------------------ entry points

@@ -71,7 +71,9 @@ GemmParams dense_params(mmq_type t, const void* W, const void* Xq, void* out, lo
         p.w8_xs = reinterpret_cast<const float*>(xb + M * K);
         p.w8_ws = reinterpret_cast<const float*>(static_cast<const uint8_t*>(W) + N * K);
     } else {
-        p.xds = reinterpret_cast<const float4*>(xb + M * K);
+        const Q81Layout L = q81_layout(M, K);
+        p.xds = reinterpret_cast<const float4*>(xb + L.ds);
+        p.xh = reinterpret_cast<const uint16_t*>(xb + L.h);
     }
     p.out = out;
     p.w_row_bytes = weight_row_bytes(t, K);
@@ -125,8 +127,8 @@ const char* mmq_status_string(mmq_status s) {
 }
 
 size_t mmq_q8_1_bytes(int64_t M, int64_t K) {
-    if (M < 0 || K < 0 || K % 32 != 0) return 0;
-    return (size_t)(M * K + M * (K / 32) * 8);
+    if (M < 0 || K < 0 || K % 64 != 0) return 0;
+    return (size_t)q81_layout(M, K).total;
 }
 
 size_t mmq_weight_bytes(mmq_type t, int64_t N, int64_t K) {
@@ -142,8 +144,17 @@ size_t mmq_w8a8_act_bytes(int64_t M, int64_t K) {
     return (size_t)(M * K + 4 * M);
 }
 
+mmq_status mmq_q8_1_prepare(void* xq, int64_t M, int64_t K, mmq_stream_t stream) {
+    if (M < 0 || K <= 0 || K % 64 != 0 || M * K > kMaxDim) return MMQ_ERR_SHAPE;
+    if (M == 0) return MMQ_OK;
+    if (!xq) return MMQ_ERR_INVALID_ARG;
+    if (!aligned16(xq)) return MMQ_ERR_ALIGN;
+    const cudaError_t e = run_prepare_q8_1(xq, M, K, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_q8_1_prepare");
+}
+
 mmq_status mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, void* xq, mmq_stream_t stream) {
-    if (M < 0 || K <= 0 || K % 32 != 0 || M * K > kMaxDim) return MMQ_ERR_SHAPE;
+    if (M < 0 || K <= 0 || K % 64 != 0 || M * K > kMaxDim) return MMQ_ERR_SHAPE;
     if (M == 0) return MMQ_OK;
     if (!x || !xq) return MMQ_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xq)) return MMQ_ERR_ALIGN;

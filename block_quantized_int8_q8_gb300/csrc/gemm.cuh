@@ -40,7 +40,8 @@ constexpr int BM = 128;             // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;             // tokens per tile (MMA N)
 constexpr int BK = 64;              // k per pipeline stage: one 128-byte swizzle row of fp16
 constexpr int STAGES = 4;           // smem operand pipeline depth
-constexpr int SC_STAGES = 8;        // scale ring depth (released by the epilogue, so deeper)
+constexpr int SC_STAGES = 6;        // scale ring depth (released by the epilogue, so deeper)
+constexpr int RAW_STAGES = 3;       // raw-byte ring filled by cp.async, two stages ahead of conversion
 constexpr int NACC = 4;             // TMEM accumulators (BN columns each)
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_PROD_WARPS = 4;
@@ -55,25 +56,13 @@ constexpr int A_STAGE_BYTES = BM * 128;
 constexpr int B_STAGE_BYTES = BN * 128;
 constexpr int SC_STAGE_FLOATS = 2 * BM + 2 * BM + 2 * BN + 2 * BN;   // wsc, wmn, xd, xs for 2 blocks
 
-struct SmemLayout {
-    static constexpr int a_off = 0;
-    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
-    static constexpr int sc_off = b_off + STAGES * B_STAGE_BYTES;
-    static constexpr int orow_off = sc_off + SC_STAGES * SC_STAGE_FLOATS * 4;
-    static constexpr int trow_off = orow_off + BN * 4;
-    static constexpr int bar_off = trow_off + BN * 4;           // 8-byte aligned
-    static constexpr int n_bars = 2 * STAGES + 2 * SC_STAGES + 2 * NACC + 1;
-    static constexpr int misc_off = bar_off + n_bars * 8;       // tmem slot, abort flag
-    static constexpr int total = misc_off + 16;
-    static constexpr int alloc = total + 1024;                  // slack for 1024-byte alignment
-};
-
 struct GemmParams {
     const uint8_t* W;           // raw weights (expert 0 for MoE); W8A8: int8 [N][K]
     const int8_t* xq;           // activation codes [M][K]
     const float4* xds;          // q8_1 (d, s) pairs [M][K/32], read two blocks at a time
     const float* w8_ws;         // W8A8 per-channel scales [N]
     const float* w8_xs;         // W8A8 per-token scales [M]
+    const uint16_t* xh;         // q8_1 shadow: fp16 codes [M][K] (block types)
     void* out;                  // f32 [rows][N] (bf16 for W8A8)
     int32_t* partials;          // debug: int32 [M][N][groups]
     long long w_row_bytes;      // bytes per weight row
@@ -92,43 +81,53 @@ struct RawA {
     uint32_t w[17];
 };
 
+// Geometry of one weight row's raw bytes for one 64-k stage, as staged in shared memory.
+// kWords: 32-bit words of data; kVec16: copied and read as 16-byte pieces (else 4-byte words);
+// kStride: bytes between rows in the raw ring (an odd number of words / 16-byte units, so that one
+// thread per row reads without bank conflicts).
+template <int WT> struct RawGeom;
+template <> struct RawGeom<0> { static constexpr int kWords = 17, kStride = 68, kVec16 = 0; };   // Q8_0: two 34 B blocks
+template <> struct RawGeom<1> { static constexpr int kWords = 9, kStride = 36, kVec16 = 0; };    // Q4_0: two 18 B blocks
+template <> struct RawGeom<2> { static constexpr int kWords = 12, kStride = 48, kVec16 = 1; };   // Q4_K: header + 32 code bytes
+template <> struct RawGeom<3> { static constexpr int kWords = 7, kStride = 28, kVec16 = 0; };    // IQ1_M: 16 code bytes + tail
+template <> struct RawGeom<4> { static constexpr int kWords = 16, kStride = 80, kVec16 = 1; };   // W8A8: 64 int8
+
+// Shared-memory layout of one CTA, per weight type.  Block types take the token operand as fp16 rows
+// straight from the q8_1 buffer's shadow section (cp.async into the swizzled tile); W8A8 stages its
+// int8 activation rows in the raw ring and converts them.
 template <int WT>
-__device__ __forceinline__ void load_raw_a(RawA& r, const uint8_t* row, int s, bool valid) {
-    if (!valid) {
-#pragma unroll
-        for (int i = 0; i < 17; i++) r.w[i] = 0;
-        return;
-    }
-    if constexpr (WT == WT_Q8_0) {            // two 34-byte blocks: 68 bytes at 68*s (4-aligned)
-        const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 68 * s);
-#pragma unroll
-        for (int i = 0; i < 17; i++) r.w[i] = __ldg(p + i);
-    } else if constexpr (WT == WT_Q4_0) {     // two 18-byte blocks: 36 bytes at 36*s
-        const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 36 * s);
-#pragma unroll
-        for (int i = 0; i < 9; i++) r.w[i] = __ldg(p + i);
-    } else if constexpr (WT == WT_Q4_K) {     // 16-byte super-block header + the stage's 32 code bytes
+struct SmemLayoutT {
+    static constexpr bool kW8 = WT == WT_W8A8;
+    static constexpr int raw_b = kW8 ? BN * 64 : 0;              // int8 codes per token row
+    static constexpr int raw_ds = kW8 ? 0 : BN * 16;             // (d, s) of the stage's two blocks
+    static constexpr int raw_a = BM * RawGeom<WT>::kStride;
+    static constexpr int raw_stage = (raw_b + raw_ds + raw_a + 127) / 128 * 128;
+    static constexpr int a_off = 0;
+    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr int sc_off = b_off + STAGES * B_STAGE_BYTES;
+    static constexpr int raw_off = sc_off + (kW8 ? 0 : SC_STAGES * SC_STAGE_FLOATS * 4);
+    static constexpr int orow_off = raw_off + RAW_STAGES * raw_stage;
+    static constexpr int trow_off = orow_off + BN * 4;
+    static constexpr int bar_off = trow_off + BN * 4;           // 8-byte aligned
+    static constexpr int n_bars = 2 * STAGES + 2 * SC_STAGES + 2 * NACC + 1;
+    static constexpr int misc_off = bar_off + n_bars * 8;       // tmem slot, abort flag
+    static constexpr int total = misc_off + 16;
+    static constexpr int alloc = total + 1024;                  // slack for 1024-byte alignment
+};
+
+// Global address of word / 16-byte piece `i` of a weight row's raw bytes for stage s.
+template <int WT>
+__device__ __forceinline__ const uint8_t* raw_a_src(const uint8_t* row, int s, int i) {
+    if constexpr (WT == WT_Q8_0) return row + 68 * s + 4 * i;
+    else if constexpr (WT == WT_Q4_0) return row + 36 * s + 4 * i;
+    else if constexpr (WT == WT_Q4_K) {
         const uint8_t* sb = row + 144 * (s >> 2);
-        const uint4 h = __ldg(reinterpret_cast<const uint4*>(sb));
-        const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(sb + 16 + 32 * (s & 3)));
-        const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(sb + 32 + 32 * (s & 3)));
-        r.w[0] = h.x; r.w[1] = h.y; r.w[2] = h.z; r.w[3] = h.w;
-        r.w[4] = c0.x; r.w[5] = c0.y; r.w[6] = c0.z; r.w[7] = c0.w;
-        r.w[8] = c1.x; r.w[9] = c1.y; r.w[10] = c1.z; r.w[11] = c1.w;
-    } else if constexpr (WT == WT_IQ1_M) {    // the stage's 16 code bytes + signs/sub-scales/d (12 bytes)
-        const uint32_t* sb = reinterpret_cast<const uint32_t*>(row + 76 * (s >> 2));
-#pragma unroll
-        for (int i = 0; i < 4; i++) r.w[i] = __ldg(sb + 4 * (s & 3) + i);
-        r.w[4] = __ldg(sb + 16);
-        r.w[5] = __ldg(sb + 17);
-        r.w[6] = __ldg(sb + 18);
-    } else {                                   // W8A8: 64 int8
-        const uint4* p = reinterpret_cast<const uint4*>(row + 64 * s);
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const uint4 v = __ldg(p + i);
-            r.w[4 * i] = v.x; r.w[4 * i + 1] = v.y; r.w[4 * i + 2] = v.z; r.w[4 * i + 3] = v.w;
-        }
+        return i == 0 ? sb : sb + 16 + 32 * (s & 3) + 16 * (i - 1);
+    } else if constexpr (WT == WT_IQ1_M) {
+        const uint8_t* sb = row + 76 * (s >> 2);
+        return i < 4 ? sb + 16 * (s & 3) + 4 * i : sb + 64 + 4 * (i - 4);
+    } else {
+        return row + 64 * s + 16 * i;
     }
 }
 
@@ -239,6 +238,7 @@ struct KTraits {
 template <int WT, int MODE, bool MOE>
 __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams p) {
     using T = KTraits<WT, MODE>;
+    using SmemLayout = SmemLayoutT<WT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // align by pointer arithmetic on the __shared__ array so that the compiler keeps the address space
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -323,77 +323,124 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
 
     if (warp >= PROD_WARP0 && warp < MMA_WARP) {
         // =========================================================== producers
-        const int r = threadIdx.x - PROD_WARP0 * 32;            // row of A and of B this thread fills
-        const int n = n0 + r;
-        const bool a_valid = n < p.N;
-        const uint8_t* arow = Wbase + (long long)(a_valid ? n : 0) * p.w_row_bytes;
-        const int tr = trow[r];
-        const bool b_valid = tr >= 0;
-        const int8_t* brow = p.xq + (long long)(b_valid ? tr : 0) * p.K;
-        const float4* bds = p.xds + (long long)(b_valid ? tr : 0) * (kb32 / 2);
-        const uint32_t a_smem = smem_u32(smem + SmemLayout::a_off);
-        const uint32_t b_smem = smem_u32(smem + SmemLayout::b_off);
+        // Raw bytes arrive by coalesced cp.async into a RAW_STAGES-deep ring (issued two stages
+        // ahead, zero-filled for ragged rows); each stage is then unpacked from shared memory into
+        // the fp16 operand tiles.  Row maps and layouts: one weight row per thread for the unpack,
+        // four threads per token row for the codes.
+        using G = RawGeom<WT>;
+        const int pt = threadIdx.x - PROD_WARP0 * 32;           // 0..127
+        const uint32_t a_smem = smem_s + SmemLayout::a_off;
+        const uint32_t b_smem = smem_s + SmemLayout::b_off;
+        const uint32_t raw0 = smem_s + SmemLayout::raw_off;
+        const uint32_t trow_s = smem_s + SmemLayout::trow_off;
+        const uint8_t* xds_bytes = reinterpret_cast<const uint8_t*>(p.xds);
 
-        // Two register sets of raw bytes: the loads for stage s+1 are in flight while stage s is
-        // unpacked and stored.
-        struct RawSet {
-            RawA a;
-            uint4 b[4];
-            float4 ds;
-        };
-        auto load_stage = [&](RawSet& rs, int s) {
-            load_raw_a<WT>(rs.a, arow, s, a_valid);
-            if (b_valid) {
-                const uint4* qp = reinterpret_cast<const uint4*>(brow + 64 * s);
+        auto issue_copies = [&](int s) {
+            const uint32_t rb = raw0 + (s % RAW_STAGES) * SmemLayout::raw_stage;
+            if constexpr (SmemLayout::kW8) {                    // int8 activation rows: 512 x 16 B
 #pragma unroll
-                for (int i = 0; i < 4; i++) rs.b[i] = __ldg(qp + i);
-                if constexpr (T::kScaleRing) rs.ds = __ldg(bds + s);
-                else rs.ds = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < 4; k++) {
+                    const int i = pt + 128 * k, row = i >> 2, ch = i & 3;
+                    const int tr = ld_shared_s32(trow_s + 4 * row);
+                    const int8_t* src = p.xq + (long long)(tr >= 0 ? tr : 0) * p.K + 64 * s + 16 * ch;
+                    cp_async_16(rb + 16 * i, src, tr >= 0 ? 16u : 0u);
+                }
+            } else {
+                // fp16 token rows go straight into the operand tile once the MMA has released it:
+                // 1024 x 16 B, eight threads per row, each chunk to its 128B-swizzled position
+                const int slot = s % STAGES;
+                mbar_wait(bar_empty(slot), ((s / STAGES) & 1) ^ 1, abort_flag);
+                const uint32_t bt = b_smem + slot * B_STAGE_BYTES;
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const int i = pt + 128 * k, row = i >> 3, c = i & 7;
+                    const int tr = ld_shared_s32(trow_s + 4 * row);
+                    const uint16_t* src = p.xh + (long long)(tr >= 0 ? tr : 0) * p.K + 64 * s + 8 * c;
+                    cp_async_16(bt + sw128_off(row, c), src, tr >= 0 ? 16u : 0u);
+                }
+                if constexpr (T::kScaleRing) {                  // (d, s) of the stage's two blocks
+                    const int tr = ld_shared_s32(trow_s + 4 * pt);
+                    const uint8_t* src = xds_bytes + ((long long)(tr >= 0 ? tr : 0) * kb32 + 2 * s) * 8;
+                    cp_async_16(rb + 16 * pt, src, tr >= 0 ? 16u : 0u);
+                }
+            }
+            const uint32_t ra = rb + SmemLayout::raw_b + SmemLayout::raw_ds;
+            if constexpr (G::kVec16) {
+                constexpr int P = G::kWords / 4;
+#pragma unroll
+                for (int k = 0; k < P; k++) {
+                    const int i = pt + 128 * k, row = i / P, pc = i % P;
+                    const bool ok = n0 + row < p.N;
+                    const uint8_t* src = raw_a_src<WT>(Wbase + (long long)(ok ? n0 + row : 0) * p.w_row_bytes, s, pc);
+                    cp_async_16(ra + row * G::kStride + 16 * pc, src, ok ? 16u : 0u);
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; i++) rs.b[i] = make_uint4(0u, 0u, 0u, 0u);
-                rs.ds = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < G::kWords; k++) {
+                    const int i = pt + 128 * k, row = i / G::kWords, wd = i % G::kWords;
+                    const bool ok = n0 + row < p.N;
+                    const uint8_t* src = raw_a_src<WT>(Wbase + (long long)(ok ? n0 + row : 0) * p.w_row_bytes, s, wd);
+                    cp_async_4(ra + row * G::kStride + 4 * wd, src, ok ? 4u : 0u);
+                }
             }
         };
-        auto produce = [&](RawSet& rs, int s) {
+
+        auto convert = [&](int s) {
             const int slot = s % STAGES;
-            const uint32_t par = ((s / STAGES) & 1) ^ 1;
             const int sslot = s % SC_STAGES;
             if constexpr (T::kScaleRing) mbar_wait(bar_sfree(sslot), ((s / SC_STAGES) & 1) ^ 1, abort_flag);
-            mbar_wait(bar_empty(slot), par, abort_flag);
+            if constexpr (SmemLayout::kW8) mbar_wait(bar_empty(slot), ((s / STAGES) & 1) ^ 1, abort_flag);
+            const uint32_t rb = raw0 + (s % RAW_STAGES) * SmemLayout::raw_stage;
+            const uint32_t ra = rb + SmemLayout::raw_b + SmemLayout::raw_ds + pt * G::kStride;
             const uint32_t at = a_smem + slot * A_STAGE_BYTES;
             const uint32_t bt = b_smem + slot * B_STAGE_BYTES;
             {
+                RawA w;
+                if constexpr (G::kVec16) {
+#pragma unroll
+                    for (int k = 0; k < G::kWords / 4; k++) {
+                        const uint4 v = ld_shared_u4(ra + 16 * k);
+                        w.w[4 * k] = v.x; w.w[4 * k + 1] = v.y; w.w[4 * k + 2] = v.z; w.w[4 * k + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < G::kWords; k++) w.w[k] = ld_shared_u32(ra + 4 * k);
+                }
                 uint32_t ha[32];
                 float wsc[2], wmn[2];
-                unpack_a<WT, T::kFold>(rs.a, s, ha, wsc, wmn);
-                if (!a_valid) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
+                unpack_a<WT, T::kFold>(w, s, ha, wsc, wmn);
+                if (n0 + pt >= p.N) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
 #pragma unroll
                 for (int c = 0; c < 8; c++)
-                    st_shared_v4(at + sw128_off(r, c), ha[4 * c], ha[4 * c + 1], ha[4 * c + 2], ha[4 * c + 3]);
+                    st_shared_v4(at + sw128_off(pt, c), ha[4 * c], ha[4 * c + 1], ha[4 * c + 2], ha[4 * c + 3]);
                 if constexpr (T::kScaleRing) {
-                    const uint32_t sc = smem_s + SmemLayout::sc_off + sslot * SC_STAGE_FLOATS * 4 + 4 * r;
+                    const float4 ds = ld_shared_f4(rb + 16 * pt);
+                    const uint32_t sc = smem_s + SmemLayout::sc_off + sslot * SC_STAGE_FLOATS * 4 + 4 * pt;
                     st_shared_f32(sc + 4 * (0 * BM), wsc[0]);
                     st_shared_f32(sc + 4 * (1 * BM), wsc[1]);
                     st_shared_f32(sc + 4 * (2 * BM), wmn[0]);
                     st_shared_f32(sc + 4 * (3 * BM), wmn[1]);
-                    st_shared_f32(sc + 4 * (4 * BM), rs.ds.x);              // xd, block 0
-                    st_shared_f32(sc + 4 * (4 * BM + BN), rs.ds.z);         // xd, block 1
-                    st_shared_f32(sc + 4 * (4 * BM + 2 * BN), rs.ds.y);     // xs, block 0
-                    st_shared_f32(sc + 4 * (4 * BM + 3 * BN), rs.ds.w);     // xs, block 1
+                    st_shared_f32(sc + 4 * (4 * BM), ds.x);               // xd, block 0
+                    st_shared_f32(sc + 4 * (4 * BM + BN), ds.z);          // xd, block 1
+                    st_shared_f32(sc + 4 * (4 * BM + 2 * BN), ds.y);      // xs, block 0
+                    st_shared_f32(sc + 4 * (4 * BM + 3 * BN), ds.w);      // xs, block 1
                 }
             }
+            if constexpr (SmemLayout::kW8) {
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                uint32_t hb[8];
-                s8x4_to_f16x4(rs.b[i].x, hb[0], hb[1]);
-                s8x4_to_f16x4(rs.b[i].y, hb[2], hb[3]);
-                s8x4_to_f16x4(rs.b[i].z, hb[4], hb[5]);
-                s8x4_to_f16x4(rs.b[i].w, hb[6], hb[7]);
-                st_shared_v4(bt + sw128_off(r, 2 * i), hb[0], hb[1], hb[2], hb[3]);
-                st_shared_v4(bt + sw128_off(r, 2 * i + 1), hb[4], hb[5], hb[6], hb[7]);
+                for (int k = 0; k < 4; k++) {                      // W8A8 activation codes -> fp16
+                    const int i = pt + 128 * k, row = i >> 2, ch = i & 3;
+                    const uint4 q = ld_shared_u4(rb + 16 * i);
+                    uint32_t hb[8];
+                    s8x4_to_f16x4(q.x, hb[0], hb[1]);
+                    s8x4_to_f16x4(q.y, hb[2], hb[3]);
+                    s8x4_to_f16x4(q.z, hb[4], hb[5]);
+                    s8x4_to_f16x4(q.w, hb[6], hb[7]);
+                    st_shared_v4(bt + sw128_off(row, 2 * ch), hb[0], hb[1], hb[2], hb[3]);
+                    st_shared_v4(bt + sw128_off(row, 2 * ch + 1), hb[4], hb[5], hb[6], hb[7]);
+                }
             }
-            fence_proxy_async_smem();       // this thread's tile stores -> visible to the tensor core
+            fence_proxy_async_smem();       // this thread's tile stores and landed copies -> tensor core
             __syncwarp();
             if ((threadIdx.x & 31) == 0) {
                 mbar_arrive(bar_full(slot));
@@ -401,17 +448,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
             }
         };
 
-        RawSet set0, set1;
-        load_stage(set0, 0);
-        if (nstages > 1) load_stage(set1, 1);
-        for (int s = 0; s < nstages; s += 2) {
-            produce(set0, s);
-            if (s + 2 < nstages) load_stage(set0, s + 2);
-            if (s + 1 < nstages) {
-                produce(set1, s + 1);
-                if (s + 3 < nstages) load_stage(set1, s + 3);
-            }
+        // prologue: RAW_STAGES groups (empty ones past the end keep the group count uniform)
+#pragma unroll 1
+        for (int t = 0; t < RAW_STAGES; t++) {
+            if (t < nstages) issue_copies(t);
+            cp_async_commit();
         }
+#pragma unroll 1
+        for (int s = 0; s < nstages; s++) {
+            if (s == 0) cp_async_wait<RAW_STAGES - 1>();
+            else cp_async_wait<RAW_STAGES - 2>();
+            // every producer thread's copies of stage s have landed, and every producer thread has
+            // finished unpacking stage s-1, whose raw slot is refilled next
+            named_bar_sync(1, NUM_PROD_WARPS * 32);
+            if (s >= 1) {
+                if (s - 1 + RAW_STAGES < nstages) issue_copies(s - 1 + RAW_STAGES);
+                cp_async_commit();
+            }
+            convert(s);
+        }
+        cp_async_wait<0>();
     } else if (warp == MMA_WARP) {
         // =========================================================== MMA issuer
         if (lane == 0) {
@@ -578,6 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
 // ------------------------------------------------------------------------------------------ host launch
 template <int WT, int MODE, bool MOE>
 cudaError_t launch_gemm(const GemmParams& p, int grid_y, cudaStream_t stream) {
+    using SmemLayout = SmemLayoutT<WT>;
     static bool configured = false;
     auto kern = mmq_gemm_kernel<WT, MODE, MOE>;
     if (!configured) {

@@ -6,8 +6,22 @@
 namespace mmq {
 struct GemmParams;
 
-// Quantizer (quantize.cu)
+// q8_1 buffer sections (byte offsets), see include/mmq.h
+struct Q81Layout {
+    long long ds, h, xs3, total;
+};
+inline Q81Layout q81_layout(long long M, long long K) {
+    Q81Layout L;
+    L.ds = M * K;
+    L.h = (M * K + M * (K / 32) * 8 + 255) / 256 * 256;
+    L.xs3 = L.h + 2 * M * K;
+    L.total = (L.xs3 + M * (K / 32) * 16 + 255) / 256 * 256;
+    return L;
+}
+
+// Quantizer and shadow preparation (quantize.cu)
 cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq, cudaStream_t s);
+cudaError_t run_prepare_q8_1(void* xq, long long M, long long K, cudaStream_t s);
 
 // Dense / MoE / debug GEMM launchers, one per weight type (gemm_<type>.cu).
 // mode: 0 production, 1 debug partials.  moe: grouped launch driven by the routing workspace.

@@ -3,13 +3,15 @@
 // Per 32-value block: amax = max|x|, d = amax/127, q = round-half-even(x/d) (correctly rounded f32
 // division), s = d * sum(q)  ("08 · R1 — int8 MMQ prefill GEMM", §2.2 q8_1 activation pipeline, and
 // the §3.2 reference quantizer; f32 scale, the block sum produced in the same pass).
-// Output layout: int8 q[M][K] at byte 0, then float2 (d, s)[M][K/32].
+// Output layout (include/mmq.h): int8 q[M][K], float2 (d, s)[M][K/32], then the tensor-core shadow:
+// fp16 h[M][K] = q exactly, and bf16 {x1,x1,x2,x2,x3,x3,0,0} per block with x1 + x2 + x3 = d exactly.
 //
 // HBM-bound: 4 bytes read and 1.25 bytes written per value.  Eight lanes own one block (one float4
 // each); amax and sum(q) are warp-shuffle reductions over the eight lanes; every lane stores its
 // four codes as one 32-bit word, so a warp writes 128 contiguous bytes per block quad.
 #include <cstdint>
 #include "internal.h"
+#include <cuda_fp16.h>
 #include "mmq_device.cuh"
 
 namespace mmq {
@@ -23,13 +25,32 @@ __device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
     return v;
 }
 
+// d = x1 + x2 + x3 exactly, each a bf16: x1 keeps d's top 16 bits, x2 the remainder's top 16 bits,
+// and the last remainder has at most 8 significant bits.  Returned as the 16-byte block record.
+__device__ __forceinline__ uint4 split3_record(float d) {
+    const float x1 = __uint_as_float(__float_as_uint(d) & 0xFFFF0000u);
+    const float r1 = __fsub_rn(d, x1);
+    const float x2 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
+    const float x3 = __fsub_rn(r1, x2);
+    const uint32_t h1 = __float_as_uint(x1) >> 16, h2 = __float_as_uint(x2) >> 16, h3 = __float_as_uint(x3) >> 16;
+    return make_uint4(h1 | (h1 << 16), h2 | (h2 << 16), h3 | (h3 << 16), 0u);
+}
+
+// four codes -> four fp16 (exact)
+__device__ __forceinline__ uint2 codes_to_f16x4(int q0, int q1, int q2, int q3) {
+    const __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+    const __half2 b = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
 __device__ __forceinline__ int q8_code(float x, float d) {
     const int q = __float2int_rn(__fdiv_rn(x, d));        // ties to even
     return max(-127, min(127, q));
 }
 
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, uint32_t* __restrict__ q,
-                                                           float2* __restrict__ ds, long long nblk) {
+                                                           float2* __restrict__ ds, uint2* __restrict__ h,
+                                                           uint4* __restrict__ xs3, long long nblk) {
     const int lane = threadIdx.x & 31, sub = lane & 7, grp = lane >> 3;
     const long long warp_id = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (gridDim.x * (long long)blockDim.x) >> 5;
@@ -63,7 +84,11 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
             if (blk < nblk) {
                 q[blk * 8 + sub] = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
                                    ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
-                if (sub == 0) ds[blk] = make_float2(d, __fmul_rn(d, (float)sum));
+                h[blk * 8 + sub] = codes_to_f16x4(q0, q1, q2, q3);
+                if (sub == 0) {
+                    ds[blk] = make_float2(d, __fmul_rn(d, (float)sum));
+                    xs3[blk] = split3_record(d);
+                }
             }
         }
     }
@@ -80,9 +105,40 @@ cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq
     const long long cap = (long long)sms * 8;              // 8 x 256 threads resident per SM
     if (blocks > cap) blocks = cap;
     uint8_t* base = static_cast<uint8_t*>(xq);
-    quantize_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(x),
-                                                          reinterpret_cast<uint32_t*>(base),
-                                                          reinterpret_cast<float2*>(base + M * K), nblk);
+    const Q81Layout L = q81_layout(M, K);
+    quantize_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+        reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(base), reinterpret_cast<float2*>(base + L.ds),
+        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3), nblk);
+    return cudaGetLastError();
+}
+
+// Derived sections from existing q8_1 blocks: eight lanes per block, one 32-bit word of codes each.
+__global__ void __launch_bounds__(256) prepare_q8_1_kernel(const uint32_t* __restrict__ q,
+                                                          const float2* __restrict__ ds, uint2* __restrict__ h,
+                                                          uint4* __restrict__ xs3, long long nblk) {
+    const long long stride = (gridDim.x * (long long)blockDim.x) >> 3;
+    const int sub = threadIdx.x & 7;
+    for (long long blk = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3; blk < nblk; blk += stride) {
+        const uint32_t w = q[blk * 8 + sub];
+        h[blk * 8 + sub] = codes_to_f16x4((int)(int8_t)(w & 0xff), (int)(int8_t)((w >> 8) & 0xff),
+                                          (int)(int8_t)((w >> 16) & 0xff), (int)(int8_t)(w >> 24));
+        if (sub == 0) xs3[blk] = split3_record(ds[blk].x);
+    }
+}
+
+cudaError_t run_prepare_q8_1(void* xq, long long M, long long K, cudaStream_t s) {
+    const long long nblk = M * K / 32;
+    if (nblk == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long blocks = (nblk * 8 + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    uint8_t* base = static_cast<uint8_t*>(xq);
+    const Q81Layout L = q81_layout(M, K);
+    prepare_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+        reinterpret_cast<const uint32_t*>(base), reinterpret_cast<const float2*>(base + L.ds),
+        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3), nblk);
     return cudaGetLastError();
 }
 

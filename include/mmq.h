@@ -23,9 +23,16 @@
  *     a device-resident error word that mmq_read_device_errors() returns and clears.
  *
  * Byte layouts (this library's; the pages give block sizes, not bit layouts):
- *   q8_1 activations (mmq_q8_1_bytes(M,K) = 40*M*K/32 bytes):
- *       int8 q[M][K]                    at byte 0
- *       float2 ds[M][K/32] = (d, s)     at byte M*K
+ *   q8_1 activations (mmq_q8_1_bytes(M,K) bytes), four sections:
+ *       int8 q[M][K]                    at byte 0            the q8_1 codes
+ *       float2 ds[M][K/32] = (d, s)     at byte M*K          per-block scale and block sum
+ *       fp16 h[M][K]                    at byte H = round_up(M*K + 8*M*K/32, 256)
+ *                                                            h = q exactly (tensor-core operand)
+ *       bf16 xs3[M][K/32][8]            at byte H + 2*M*K    per block {x1,x1,x2,x2,x3,x3,0,0}
+ *                                                            with x1 + x2 + x3 = d exactly (x1, x2 are
+ *                                                            d and its remainder truncated to bf16)
+ *       The first two sections are the q8_1 blocks (40 B per 32 values); the last two are derived
+ *       from them (mmq_q8_1_prepare) so that the GEMM reads tensor-core-ready operands.
  *   Q8_0  34 B / 32 values : f16 d | int8 q[32]                        value = d*q
  *   Q4_0  18 B / 32 values : f16 d | 16 B, byte i = code i (low nibble) | code i+16 (high nibble)
  *                            value = d*(code-8)
@@ -88,7 +95,7 @@ const char* mmq_status_string(mmq_status s);
  * host thread ("" if none).  The string stays valid until the next failing call on that thread. */
 const char* mmq_last_cuda_error(void);
 
-/* Bytes of a q8_1 activation buffer for an [M][K] matrix: 40*M*K/32. */
+/* Bytes of a q8_1 activation buffer for an [M][K] matrix, all four sections (K % 64 == 0). */
 size_t mmq_q8_1_bytes(int64_t M, int64_t K);
 
 /* Bytes of a raw weight buffer of type t with N rows of K values (W8A8: N*K + 4*N). 0 on bad args. */
@@ -103,9 +110,16 @@ size_t mmq_w8a8_act_bytes(int64_t M, int64_t K);
  * xq  : output q8_1 buffer of mmq_q8_1_bytes(M, K) bytes, device.
  * Per row and 32-value block: amax = max|x|; d = amax/127 (f32, round to nearest); q = round-half-even
  * of the correctly rounded f32 x/d, clamped to [-127,127]; s = d*(float)sum(q).  amax == 0 gives
- * d = 0, q = 0, s = 0.  Inputs must be finite.  K % 32 == 0.
+ * d = 0, q = 0, s = 0.  Inputs must be finite.  K % 64 == 0.  Writes all four sections.
  */
 mmq_status mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, void* xq, mmq_stream_t stream);
+
+/*
+ * mmq_q8_1_prepare -- fill the two derived sections (h, xs3) of a q8_1 buffer from its q and ds
+ * sections, for callers that produce q8_1 blocks themselves.  mmq_quantize_q8_1 already does this.
+ * Exact: h = q as fp16; x1 = d truncated to bf16, x2 = (d - x1) truncated to bf16, x3 = d - x1 - x2.
+ */
+mmq_status mmq_q8_1_prepare(void* xq, int64_t M, int64_t K, mmq_stream_t stream);
 
 /*
  * mmq_gemm -- dense MMQ product ("A Negative Result on int8 Tensor-Core MMQ", §2; "08 · R1", §3.2

@@ -27,7 +27,10 @@ def test_header_declares_exactly_the_exported_api(lib):
 
 
 def test_sizes(lib):
-    assert api.q8_1_bytes(3, 64) == 3 * 64 + 3 * 2 * 8
+    o = api.q8_1_offsets(3, 64)
+    assert o["ds"] == 3 * 64 and o["h"] % 256 == 0 and o["h"] >= 3 * 64 + 3 * 2 * 8
+    assert api.q8_1_bytes(3, 64) >= o["xs3"] + 3 * 2 * 16 and api.q8_1_bytes(3, 64) % 256 == 0
+    assert api.q8_1_bytes(3, 32) == 0                     # K % 64 required
     assert api.weight_bytes(api.Q8_0, 5, 256) == 5 * 8 * 34
     assert api.weight_bytes(api.Q4_0, 5, 256) == 5 * 8 * 18
     assert api.weight_bytes(api.Q4_K, 5, 512) == 5 * 2 * 144
@@ -56,8 +59,10 @@ def test_gemm_argument_validation(lib, args, status):
 
 def test_quantize_and_gemm_id_validation(lib):
     assert lib.mmq_quantize_q8_1(FAKE, 4, 33, FAKE, None) == 2
-    assert lib.mmq_quantize_q8_1(None, 4, 32, FAKE, None) == 1
-    assert lib.mmq_quantize_q8_1(FAKE, 4, 32, FAKE + 8, None) == 3
+    assert lib.mmq_quantize_q8_1(None, 4, 64, FAKE, None) == 1
+    assert lib.mmq_quantize_q8_1(FAKE, 4, 64, FAKE + 8, None) == 3
+    assert lib.mmq_q8_1_prepare(FAKE, 4, 96, None) == 2
+    assert lib.mmq_q8_1_prepare(None, 4, 64, None) == 1
     ok = (api.IQ1_M, FAKE, 4, FAKE, FAKE, 2, FAKE, 16, 128, 256)
     need = api.gemm_id_workspace_bytes(16, 2, 4)
     assert lib.mmq_gemm_id(*ok, FAKE, need - 1, None) == 6          # workspace too small

@@ -39,7 +39,7 @@ def _oracle_acts(pb):
 
 
 # ---------------------------------------------------------------------------------------- quantizer
-@pytest.mark.parametrize("M,K", [(1, 32), (3, 64), (37, 4096), (257, 1024), (2048, 4096)])
+@pytest.mark.parametrize("M,K", [(1, 64), (3, 64), (37, 4096), (257, 1024), (2048, 4096)])
 def test_quantizer_bit_exact(M, K):
     g = np.random.default_rng(M * 7 + K)
     x = g.standard_normal((M, K), dtype=np.float32)
@@ -55,6 +55,29 @@ def test_quantizer_bit_exact(M, K):
     assert np.array_equal(qg.cpu().numpy(), q)
     assert np.array_equal(dsg[..., 0].cpu().numpy().view(np.uint32), d.view(np.uint32))
     assert np.array_equal(dsg[..., 1].cpu().numpy().view(np.uint32), s.view(np.uint32))
+    _check_shadow(buf, q, d, M, K)
+
+
+def _check_shadow(buf, q, d, M, K):
+    # derived sections: fp16 codes equal the int8 codes; the bf16 pieces sum exactly to d
+    h, xs3 = api.q8_1_shadow_views(buf, M, K)
+    assert np.array_equal(h.float().cpu().numpy(), q.astype(np.float32))
+    pc = xs3.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(pc[..., 0], pc[..., 1]) and np.array_equal(pc[..., 2], pc[..., 3])
+    assert np.array_equal(pc[..., 4], pc[..., 5]) and np.all(pc[..., 6:] == 0)
+    assert np.array_equal(pc[..., 0] + pc[..., 2] + pc[..., 4], d.astype(np.float64))
+
+
+def test_prepare_rebuilds_the_quantizer_shadow():
+    M, K = 130, 1024
+    x = np.random.default_rng(5).standard_normal((M, K), dtype=np.float32)
+    buf = api.quantize_q8_1(_dev(x))
+    q, d, s = oracle.quantize_q8_1(x)
+    packed = api.pack_q8_1(torch.from_numpy(q), torch.from_numpy(d), torch.from_numpy(s))
+    torch.cuda.synchronize()
+    o = api.q8_1_offsets(M, K)
+    assert torch.equal(buf[o["h"]:], packed[o["h"]:])
+    _check_shadow(packed, q, d, M, K)
 
 
 def test_quantizer_extreme_scales_bit_exact():
@@ -204,6 +227,6 @@ def test_empty_inputs_are_noops():
     out = torch.zeros(16, device=DEV)
     assert api.load().mmq_gemm(synth.Q4_0, W.data_ptr(), xq.data_ptr(), out.data_ptr(), 0, 5, 256, None) == 0
     assert api.load().mmq_gemm(synth.Q4_0, W.data_ptr(), xq.data_ptr(), out.data_ptr(), 5, 0, 256, None) == 0
-    assert api.load().mmq_quantize_q8_1(out.data_ptr(), 0, 32, xq.data_ptr(), None) == 0
+    assert api.load().mmq_quantize_q8_1(out.data_ptr(), 0, 64, xq.data_ptr(), None) == 0
     torch.cuda.synchronize()
     assert torch.all(out == 0)
