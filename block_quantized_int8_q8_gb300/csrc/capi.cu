@@ -74,6 +74,7 @@ GemmParams dense_params(mmq_type t, const void* W, const void* Xq, void* out, lo
         const Q81Layout L = q81_layout(M, K);
         p.xds = reinterpret_cast<const float4*>(xb + L.ds);
         p.xh = reinterpret_cast<const uint16_t*>(xb + L.h);
+        p.xs3 = reinterpret_cast<const uint4*>(xb + L.xs3);
     }
     p.out = out;
     p.w_row_bytes = weight_row_bytes(t, K);

@@ -33,6 +33,32 @@
 
 namespace mmq {
 
+// Scale-product operands (one 16-byte row per weight row / token per block, K-major, no swizzle).
+// The K=16 MMA reads two 8-element K chunks; the leading byte offset is 0 so both chunks are the same
+// 16 bytes, every product is counted twice, and the weight-side pieces carry a factor 1/2 (exact).
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)0 << 16;                           // leading byte offset: both K chunks alias
+    d |= (uint64_t)(128 >> 4) << 32;                  // stride byte offset: 8 rows x 16 B
+    d |= (uint64_t)1 << 46;                           // fixed 0b001 field
+    return d;                                         // swizzle mode 0: none
+}
+
+// Instruction descriptor, kind::f16 with bf16 A and B, f32 D, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// bf16 record {w1, w2, w1, w2, w1, w2, 0, 0} with w1 + w2 = v exactly (v has at most 16 significant
+// bits: an f16 scale, halved); w1 keeps v's top 16 bits.
+__device__ __forceinline__ uint4 split2_record(float v) {
+    const float w1 = __uint_as_float(__float_as_uint(v) & 0xFFFF0000u);
+    const float w2 = __fsub_rn(v, w1);
+    const uint32_t h = (__float_as_uint(w1) >> 16) | (__float_as_uint(w2) & 0xFFFF0000u);
+    return make_uint4(h, h, h, 0u);
+}
+
 enum WType { WT_Q8_0 = 0, WT_Q4_0 = 1, WT_Q4_K = 2, WT_IQ1_M = 3, WT_W8A8 = 4 };
 enum Mode { MODE_PROD = 0, MODE_DEBUG = 1 };
 
@@ -60,6 +86,7 @@ struct GemmParams {
     const uint8_t* W;           // raw weights (expert 0 for MoE); W8A8: int8 [N][K]
     const int8_t* xq;           // activation codes [M][K]
     const float4* xds;          // q8_1 (d, s) pairs [M][K/32], read two blocks at a time
+    const uint4* xs3;           // q8_1 shadow: bf16 pieces of d per block [M][K/32]
     const float* w8_ws;         // W8A8 per-channel scales [N]
     const float* w8_xs;         // W8A8 per-token scales [M]
     const uint16_t* xh;         // q8_1 shadow: fp16 codes [M][K] (block types)
@@ -95,17 +122,20 @@ template <> struct RawGeom<4> { static constexpr int kWords = 16, kStride = 80, 
 // Shared-memory layout of one CTA, per weight type.  Block types take the token operand as fp16 rows
 // straight from the q8_1 buffer's shadow section (cp.async into the swizzled tile); W8A8 stages its
 // int8 activation rows in the raw ring and converts them.
-template <int WT>
+template <int WT, bool SB, bool RING>
 struct SmemLayoutT {
     static constexpr bool kW8 = WT == WT_W8A8;
     static constexpr int raw_b = kW8 ? BN * 64 : 0;              // int8 codes per token row
-    static constexpr int raw_ds = kW8 ? 0 : BN * 16;             // (d, s) of the stage's two blocks
+    static constexpr int raw_ds = RING ? BN * 16 : 0;            // (d, s) of the stage's two blocks
     static constexpr int raw_a = BM * RawGeom<WT>::kStride;
     static constexpr int raw_stage = (raw_b + raw_ds + raw_a + 127) / 128 * 128;
+    static constexpr int sop_block = (BM + BN) * 16;             // weight-side then token-side scale rows
+    static constexpr int sop_stage = 2 * sop_block;
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
-    static constexpr int sc_off = b_off + STAGES * B_STAGE_BYTES;
-    static constexpr int raw_off = sc_off + (kW8 ? 0 : SC_STAGES * SC_STAGE_FLOATS * 4);
+    static constexpr int sop_off = b_off + STAGES * B_STAGE_BYTES;
+    static constexpr int sc_off = sop_off + (SB ? STAGES * sop_stage : 0);
+    static constexpr int raw_off = sc_off + (RING ? SC_STAGES * SC_STAGE_FLOATS * 4 : 0);
     static constexpr int orow_off = raw_off + RAW_STAGES * raw_stage;
     static constexpr int trow_off = orow_off + BN * 4;
     static constexpr int bar_off = trow_off + BN * 4;           // 8-byte aligned
@@ -182,9 +212,11 @@ __device__ __forceinline__ void unpack_a(const RawA& r, int s, uint32_t (&h)[32]
         const float dmin = half_bits_to_float((uint16_t)(r.w[0] >> 16));
         const uint32_t bits[4] = {r.w[1], r.w[2], r.w[3], 0u};
         const int j = s & 3;                                   // sub-blocks 2j, 2j+1
+        uint32_t sc[2];
 #pragma unroll
         for (int i = 0; i < 2; i++) {
-            wsc[i] = d * (float)field_le(bits, 6 * (2 * j + i), 6);
+            sc[i] = field_le(bits, 6 * (2 * j + i), 6);
+            wsc[i] = d * (float)sc[i];
             wmn[i] = dmin * (float)field_le(bits, 6 * (8 + 2 * j + i), 6);
         }
         const uint32_t bias = 0x64006400u;                     // unsigned codes 0..15
@@ -193,6 +225,17 @@ __device__ __forceinline__ void unpack_a(const RawA& r, int s, uint32_t (&h)[32]
             const uint32_t nw = r.w[4 + t];
             u8x4_to_f16x4(nw & 0x0F0F0F0Fu, bias, h[2 * t], h[2 * t + 1]);
             u8x4_to_f16x4((nw >> 4) & 0x0F0F0F0Fu, bias, h[16 + 2 * t], h[16 + 2 * t + 1]);
+        }
+        if constexpr (PROD_FOLD) {
+            // fold the 6-bit sub-block scale into the operand: sc * code <= 63 * 15, exact in fp16;
+            // the block's weight scale is then the super-block d
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const uint32_t scw = u10x2_to_f16x2(sc[i] | (sc[i] << 16), 0x64006400u);   // (sc, sc) in fp16
+#pragma unroll
+                for (int t = 0; t < 16; t++) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[16 * i + t]) : "r"(scw));
+                wsc[i] = d;
+            }
         }
     } else if constexpr (WT == WT_IQ1_M) {
         const int j = s & 3;
@@ -231,14 +274,19 @@ struct KTraits {
     static constexpr bool kIsW8 = WT == WT_W8A8;
     // k16 MMA steps per accumulator group
     static constexpr int G16 = (MODE == MODE_DEBUG) ? ((WT == WT_IQ1_M) ? 1 : 2) : (kIsW8 ? W8A8_CHUNK_K16 : 2);
-    static constexpr bool kScaleRing = (MODE == MODE_PROD) && !kIsW8;
+    // block types in production: the per-block scale product xd*wd is an MMA outer product (S)
+    static constexpr bool kSB = (MODE == MODE_PROD) && !kIsW8;
+    // Q4_K's min term -dmin*m_b*s[m,b] is applied from a shared-memory scale ring
+    static constexpr bool kScaleRing = kSB && WT == WT_Q4_K;
     static constexpr bool kFold = (MODE == MODE_PROD);
+    static constexpr int kNacc = kSB ? 2 : NACC;              // TMEM accumulators in rotation
+    static constexpr int kAccCols = kSB ? 2 * BN : BN;        // columns per accumulator: I (and S)
 };
 
 template <int WT, int MODE, bool MOE>
 __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams p) {
     using T = KTraits<WT, MODE>;
-    using SmemLayout = SmemLayoutT<WT>;
+    using SmemLayout = SmemLayoutT<WT, T::kSB, T::kScaleRing>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // align by pointer arithmetic on the __shared__ array so that the compiler keeps the address space
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -333,7 +381,44 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
         const uint32_t b_smem = smem_s + SmemLayout::b_off;
         const uint32_t raw0 = smem_s + SmemLayout::raw_off;
         const uint32_t trow_s = smem_s + SmemLayout::trow_off;
+        const uint32_t sop_smem = smem_s + SmemLayout::sop_off;
         const uint8_t* xds_bytes = reinterpret_cast<const uint8_t*>(p.xds);
+
+        // Per-thread copy addresses are fixed for the whole tile: each thread always copies the same
+        // token rows / 16-byte chunks and the same weight words; only a per-stage offset changes.
+        // token rows (block types): chunk c of rows (pt/8) + 16k, k = 0..7, into the swizzled tile
+        const int bc = pt & 7;
+        const uint32_t b_dst0 = (uint32_t)sw128_off((uint32_t)(pt >> 3), (uint32_t)bc);   // + 2048*k
+        const char* b_src[8];
+        uint32_t b_ok = 0;
+        if constexpr (!SmemLayout::kW8) {
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int tr = ld_shared_s32(trow_s + 4 * ((pt >> 3) + 16 * k));
+                b_src[k] = reinterpret_cast<const char*>(p.xh + (long long)(tr >= 0 ? tr : 0) * p.K + 8 * bc);
+                b_ok |= (tr >= 0 ? 1u : 0u) << k;
+            }
+        }
+        // this thread's own token row: scale records / (d, s) pairs / W8A8 int8 codes
+        const int my_tr = ld_shared_s32(trow_s + 4 * pt);
+        const bool my_ok = my_tr >= 0;
+        const long long my_row = my_ok ? my_tr : 0;
+        // weight words (or 16-byte pieces) i = pt + 128k: row i / words, offset within the row chunk
+        constexpr int AW = G::kVec16 ? G::kWords / 4 : G::kWords;
+        uint32_t a_off[AW];
+        uint32_t a_ok = 0;
+#pragma unroll
+        for (int k = 0; k < AW; k++) {
+            const int i = pt + 128 * k, row = i / AW, wd = i % AW;
+            const bool ok = n0 + row < p.N;
+            uint32_t o = (uint32_t)((long long)(ok ? n0 + row : 0) * p.w_row_bytes);
+            if constexpr (WT == WT_Q4_K) o += wd ? 16u * wd : 0u;              // header, then code pieces
+            else if constexpr (WT == WT_IQ1_M) o += wd < 4 ? 4u * wd : 64u + 4u * (wd - 4);
+            else if constexpr (G::kVec16) o += 16u * wd;
+            else o += 4u * wd;
+            a_off[k] = o;
+            a_ok |= (ok ? 1u : 0u) << k;
+        }
 
         auto issue_copies = [&](int s) {
             const uint32_t rb = raw0 + (s % RAW_STAGES) * SmemLayout::raw_stage;
@@ -346,41 +431,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                     cp_async_16(rb + 16 * i, src, tr >= 0 ? 16u : 0u);
                 }
             } else {
-                // fp16 token rows go straight into the operand tile once the MMA has released it:
-                // 1024 x 16 B, eight threads per row, each chunk to its 128B-swizzled position
+                // fp16 token rows go straight into the operand tile once the MMA has released it
                 const int slot = s % STAGES;
                 mbar_wait(bar_empty(slot), ((s / STAGES) & 1) ^ 1, abort_flag);
-                const uint32_t bt = b_smem + slot * B_STAGE_BYTES;
+                const uint32_t bt = b_smem + slot * B_STAGE_BYTES + b_dst0;
 #pragma unroll
-                for (int k = 0; k < 8; k++) {
-                    const int i = pt + 128 * k, row = i >> 3, c = i & 7;
-                    const int tr = ld_shared_s32(trow_s + 4 * row);
-                    const uint16_t* src = p.xh + (long long)(tr >= 0 ? tr : 0) * p.K + 64 * s + 8 * c;
-                    cp_async_16(bt + sw128_off(row, c), src, tr >= 0 ? 16u : 0u);
+                for (int k = 0; k < 8; k++)
+                    cp_async_16(bt + 2048 * k, b_src[k] + 128 * s, ((b_ok >> k) & 1) ? 16u : 0u);
+                if constexpr (T::kSB) {                         // token-side scale rows of the two blocks
+                    const uint4* src = p.xs3 + my_row * kb32 + 2 * s;
+                    const uint32_t so = sop_smem + slot * SmemLayout::sop_stage + BM * 16 + 16 * pt;
+                    cp_async_16(so, src, my_ok ? 16u : 0u);
+                    cp_async_16(so + SmemLayout::sop_block, src + 1, my_ok ? 16u : 0u);
                 }
                 if constexpr (T::kScaleRing) {                  // (d, s) of the stage's two blocks
-                    const int tr = ld_shared_s32(trow_s + 4 * pt);
-                    const uint8_t* src = xds_bytes + ((long long)(tr >= 0 ? tr : 0) * kb32 + 2 * s) * 8;
-                    cp_async_16(rb + 16 * pt, src, tr >= 0 ? 16u : 0u);
+                    const uint8_t* src = xds_bytes + (my_row * kb32 + 2 * s) * 8;
+                    cp_async_16(rb + 16 * pt, src, my_ok ? 16u : 0u);
                 }
             }
+            // weight row chunks of this stage
             const uint32_t ra = rb + SmemLayout::raw_b + SmemLayout::raw_ds;
-            if constexpr (G::kVec16) {
-                constexpr int P = G::kWords / 4;
+            uint32_t so_main, so_tail;                          // per-stage source offsets
+            if constexpr (WT == WT_Q8_0) so_main = so_tail = 68u * s;
+            else if constexpr (WT == WT_Q4_0) so_main = so_tail = 36u * s;
+            else if constexpr (WT == WT_Q4_K) { so_tail = 144u * (s >> 2); so_main = so_tail + 16u + 32u * (s & 3) - 16u; }
+            else if constexpr (WT == WT_IQ1_M) { so_tail = 76u * (s >> 2); so_main = so_tail + 16u * (s & 3); }
+            else so_main = so_tail = 64u * s;
 #pragma unroll
-                for (int k = 0; k < P; k++) {
-                    const int i = pt + 128 * k, row = i / P, pc = i % P;
-                    const bool ok = n0 + row < p.N;
-                    const uint8_t* src = raw_a_src<WT>(Wbase + (long long)(ok ? n0 + row : 0) * p.w_row_bytes, s, pc);
-                    cp_async_16(ra + row * G::kStride + 16 * pc, src, ok ? 16u : 0u);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < G::kWords; k++) {
-                    const int i = pt + 128 * k, row = i / G::kWords, wd = i % G::kWords;
-                    const bool ok = n0 + row < p.N;
-                    const uint8_t* src = raw_a_src<WT>(Wbase + (long long)(ok ? n0 + row : 0) * p.w_row_bytes, s, wd);
-                    cp_async_4(ra + row * G::kStride + 4 * wd, src, ok ? 4u : 0u);
+            for (int k = 0; k < AW; k++) {
+                const int i = pt + 128 * k;
+                uint32_t so;
+                if constexpr (WT == WT_Q4_K) so = ((i % AW) == 0) ? so_tail : so_main;
+                else if constexpr (WT == WT_IQ1_M) so = ((i % AW) < 4) ? so_main : so_tail;
+                else so = so_main;
+                const uint8_t* src = Wbase + a_off[k] + so;
+                const bool ok = (a_ok >> k) & 1;
+                if constexpr (G::kVec16) {
+                    const uint32_t dst = (WT == WT_W8A8) ? 16u * i + 16u * (uint32_t)(i >> 2) : 16u * i;
+                    cp_async_16(ra + dst, src, ok ? 16u : 0u);
+                } else {
+                    cp_async_4(ra + 4u * i, src, ok ? 4u : 0u);
                 }
             }
         };
@@ -413,6 +503,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
 #pragma unroll
                 for (int c = 0; c < 8; c++)
                     st_shared_v4(at + sw128_off(pt, c), ha[4 * c], ha[4 * c + 1], ha[4 * c + 2], ha[4 * c + 3]);
+                if constexpr (T::kSB) {
+                    // weight-side scale rows {w1,w2,w1,w2,w1,w2,0,0}, w1 + w2 = wd/2 (the MMA counts
+                    // every product twice)
+                    const uint32_t so = sop_smem + slot * SmemLayout::sop_stage + 16 * pt;
+#pragma unroll
+                    for (int i = 0; i < 2; i++) {
+                        const uint4 rec = split2_record(0.5f * wsc[i]);
+                        st_shared_v4(so + i * SmemLayout::sop_block, rec.x, rec.y, rec.z, rec.w);
+                    }
+                }
                 if constexpr (T::kScaleRing) {
                     const float4 ds = ld_shared_f4(rb + 16 * pt);
                     const uint32_t sc = smem_s + SmemLayout::sc_off + sslot * SC_STAGE_FLOATS * 4 + 4 * pt;
@@ -472,8 +572,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
         // =========================================================== MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(BM, BN);
+            const uint32_t idesc_s = idesc_bf16_f32(BM, BN);
             const uint32_t a_smem = smem_u32(smem + SmemLayout::a_off);
             const uint32_t b_smem = smem_u32(smem + SmemLayout::b_off);
+            const uint32_t sop_smem = smem_s + SmemLayout::sop_off;
             for (int s = 0; s < nstages && !*abort_flag; s++) {
                 const int slot = s % STAGES;
                 if (!mbar_wait(bar_full(slot), (s / STAGES) & 1, abort_flag)) break;
@@ -483,15 +585,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                     const int ks = 4 * s + j;
                     const int kin = ks % T::G16;
                     const int g = ks / T::G16;
-                    const int buf = g % NACC;
+                    const int buf = g % T::kNacc;
                     if (kin == 0) {
-                        mbar_wait(bar_acce(buf), ((g / NACC) & 1) ^ 1, abort_flag);
+                        mbar_wait(bar_acce(buf), ((g / T::kNacc) & 1) ^ 1, abort_flag);
                         tc_fence_after();
                     }
                     const uint64_t ad = sdesc_sw128(a_smem + slot * A_STAGE_BYTES + 32 * j);
                     const uint64_t bd = sdesc_sw128(b_smem + slot * B_STAGE_BYTES + 32 * j);
-                    umma_f16(tmem_base + buf * BN, ad, bd, idesc, kin != 0 ? 1u : 0u);
-                    if (kin == T::G16 - 1 || ks == nk16 - 1) umma_commit(bar_accf(buf));
+                    const uint32_t dcol = tmem_base + buf * T::kAccCols;
+                    umma_f16(dcol, ad, bd, idesc, kin != 0 ? 1u : 0u);
+                    if (kin == T::G16 - 1 || ks == nk16 - 1) {
+                        if constexpr (T::kSB) {
+                            // S = wd (x) xd for this block: one bf16 MMA on the scale rows
+                            const uint32_t sa = sop_smem + slot * SmemLayout::sop_stage + (j >> 1) * SmemLayout::sop_block;
+                            umma_f16(dcol + BN, sdesc_rows16(sa), sdesc_rows16(sa + BM * 16), idesc_s, 0u);
+                        }
+                        umma_commit(bar_accf(buf));
+                    }
                 }
                 umma_commit(bar_empty(slot));
             }
@@ -518,11 +628,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
         }
 
         for (int g = 0; g < ngroups; g++) {
-            const int buf = g % NACC;
-            mbar_wait(bar_accf(buf), (g / NACC) & 1, abort_flag);
+            const int buf = g % T::kNacc;
+            mbar_wait(bar_accf(buf), (g / T::kNacc) & 1, abort_flag);
             tc_fence_after();
+            const uint32_t tacc = tbase + buf * T::kAccCols;
+            // Q4_K min term: row value dmin*m_b, column values s[m,b] from the scale ring
             uint32_t sc = 0;
-            float rs = 0.f, mn = 0.f;
+            float mn = 0.f;
             int slot = 0, i = 0;
             if constexpr (T::kScaleRing) {
                 const int s = g >> 1;
@@ -530,28 +642,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                 slot = s % SC_STAGES;
                 if (i == 0) mbar_wait(bar_sfull(slot), (s / SC_STAGES) & 1, abort_flag);
                 sc = smem_s + SmemLayout::sc_off + slot * SC_STAGE_FLOATS * 4;
-                rs = ld_shared_f32(sc + 4 * (i * BM + r));
-                if constexpr (WT == WT_Q4_K) mn = ld_shared_f32(sc + 4 * (2 * BM + i * BM + r));
+                mn = ld_shared_f32(sc + 4 * (2 * BM + i * BM + r));
             }
-            const uint64_t rs2 = f2_pack(rs, rs);
             const uint64_t nmn2 = f2_pack(-mn, -mn);
-            // four quarters of 16 columns; each quarter's column scales are requested before its
-            // TMEM load so that the two latencies overlap
+            // four quarters of 16 columns: the block's integer dots I and (block types) the scale
+            // products S come from TMEM; acc += I * S in packed f32 pairs
 #pragma unroll
             for (int qq = 0; qq < 4; qq++) {
-                float4 c[4], cs[4];
+                float4 cs[4];
                 if constexpr (T::kScaleRing) {
-                    const uint32_t xd = sc + 4 * (4 * BM + i * BN + 64 * ch + 16 * qq);
+                    const uint32_t xs = sc + 4 * (4 * BM + 2 * BN + i * BN + 64 * ch + 16 * qq);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; q4++) c[q4] = ld_shared_f4(xd + 16 * q4);
-                    if constexpr (WT == WT_Q4_K) {
-                        const uint32_t xs = sc + 4 * (4 * BM + 2 * BN + i * BN + 64 * ch + 16 * qq);
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; q4++) cs[q4] = ld_shared_f4(xs + 16 * q4);
-                    }
+                    for (int q4 = 0; q4 < 4; q4++) cs[q4] = ld_shared_f4(xs + 16 * q4);
                 }
-                uint32_t v[16];
-                tmem_ld16(tbase + buf * BN + 16 * qq, v);
+                uint32_t v[16], w[16];
+                tmem_ld16(tacc + 16 * qq, v);
+                if constexpr (T::kSB) tmem_ld16(tacc + BN + 16 * qq, w);
                 tmem_ld_wait();
                 if (qq == 3) {
                     tc_fence_before();
@@ -575,11 +681,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
 #pragma unroll
                     for (int q4 = 0; q4 < 4; q4++) {
                         const int j = 4 * q4, a = 8 * qq + 2 * q4;
-                        const uint64_t s01 = f2_mul(f2_pack(c[q4].x, c[q4].y), rs2);
-                        const uint64_t s23 = f2_mul(f2_pack(c[q4].z, c[q4].w), rs2);
-                        acc2[a] = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s01, acc2[a]);
-                        acc2[a + 1] = f2_fma(f2_pack(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), s23, acc2[a + 1]);
-                        if constexpr (WT == WT_Q4_K) {
+                        acc2[a] = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                         f2_pack(__uint_as_float(w[j]), __uint_as_float(w[j + 1])), acc2[a]);
+                        acc2[a + 1] = f2_fma(f2_pack(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
+                                             f2_pack(__uint_as_float(w[j + 2]), __uint_as_float(w[j + 3])), acc2[a + 1]);
+                        if constexpr (T::kScaleRing) {
                             acc2[a] = f2_fma(nmn2, f2_pack(cs[q4].x, cs[q4].y), acc2[a]);
                             acc2[a + 1] = f2_fma(nmn2, f2_pack(cs[q4].z, cs[q4].w), acc2[a + 1]);
                         }
@@ -634,7 +740,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
 // ------------------------------------------------------------------------------------------ host launch
 template <int WT, int MODE, bool MOE>
 cudaError_t launch_gemm(const GemmParams& p, int grid_y, cudaStream_t stream) {
-    using SmemLayout = SmemLayoutT<WT>;
+    using T = KTraits<WT, MODE>;
+    using SmemLayout = SmemLayoutT<WT, T::kSB, T::kScaleRing>;
     static bool configured = false;
     auto kern = mmq_gemm_kernel<WT, MODE, MOE>;
     if (!configured) {

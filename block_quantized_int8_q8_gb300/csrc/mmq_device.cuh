@@ -46,13 +46,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps in hardware until the phase completes
+// (or the hint expires) instead of spinning through issue slots other warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(200000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Bounded: returns false (and sets the
 // abort flag and the device error word) when the limit is exceeded or the CTA already aborted.
+// The abort flag and the clock are checked every 16 sleeps (each sleep is at most 0.2 ms).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (int it = 1;; it++) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if ((it & 15) != 0) continue;
         if (*abort_flag) return false;
         if (clock64() - t0 > MMQ_WAIT_LIMIT_CYCLES) {
             *abort_flag = 1;

@@ -101,6 +101,7 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
     const Q81Layout Lq = q81_layout(M, K);
     p.xds = reinterpret_cast<const float4*>(static_cast<const uint8_t*>(Xq) + Lq.ds);
     p.xh = reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(Xq) + Lq.h);
+    p.xs3 = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(Xq) + Lq.xs3);
     p.out = out;
     p.w_row_bytes = row_bytes(wtype, K);
     p.w_expert_bytes = p.w_row_bytes * N;
