@@ -570,45 +570,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
         cp_async_wait<0>();
     } else if (warp == MMA_WARP) {
         // =========================================================== MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(BM, BN);
-            const uint32_t idesc_s = idesc_bf16_f32(BM, BN);
-            const uint32_t a_smem = smem_u32(smem + SmemLayout::a_off);
-            const uint32_t b_smem = smem_u32(smem + SmemLayout::b_off);
-            const uint32_t sop_smem = smem_s + SmemLayout::sop_off;
-            for (int s = 0; s < nstages && !*abort_flag; s++) {
-                const int slot = s % STAGES;
-                if (!mbar_wait(bar_full(slot), (s / STAGES) & 1, abort_flag)) break;
-                tc_fence_after();
+        // The whole warp runs the issue loop (warp-uniform control flow keeps the descriptors in the
+        // uniform datapath); one elected lane issues each MMA and commit.
+        const uint32_t idesc = idesc_f16_f32(BM, BN);
+        const uint32_t idesc_s = idesc_bf16_f32(BM, BN);
+        const uint32_t a_smem = smem_s + SmemLayout::a_off;
+        const uint32_t b_smem = smem_s + SmemLayout::b_off;
+        const uint32_t sop_smem = smem_s + SmemLayout::sop_off;
+        for (int s = 0; s < nstages; s++) {
+            if (*abort_flag) break;
+            const int slot = s % STAGES;
+            if (!mbar_wait(bar_full(slot), (s / STAGES) & 1, abort_flag)) break;
+            tc_fence_after();
+            const uint64_t ad0 = sdesc_sw128(a_smem + slot * A_STAGE_BYTES);
+            const uint64_t bd0 = sdesc_sw128(b_smem + slot * B_STAGE_BYTES);
 #pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const int ks = 4 * s + j;
-                    const int kin = ks % T::G16;
-                    const int g = ks / T::G16;
-                    const int buf = g % T::kNacc;
-                    if (kin == 0) {
-                        mbar_wait(bar_acce(buf), ((g / T::kNacc) & 1) ^ 1, abort_flag);
-                        tc_fence_after();
-                    }
-                    const uint64_t ad = sdesc_sw128(a_smem + slot * A_STAGE_BYTES + 32 * j);
-                    const uint64_t bd = sdesc_sw128(b_smem + slot * B_STAGE_BYTES + 32 * j);
-                    const uint32_t dcol = tmem_base + buf * T::kAccCols;
-                    umma_f16(dcol, ad, bd, idesc, kin != 0 ? 1u : 0u);
-                    if (kin == T::G16 - 1 || ks == nk16 - 1) {
-                        if constexpr (T::kSB) {
-                            // S = wd (x) xd for this block: one bf16 MMA on the scale rows
-                            const uint32_t sa = sop_smem + slot * SmemLayout::sop_stage + (j >> 1) * SmemLayout::sop_block;
-                            umma_f16(dcol + BN, sdesc_rows16(sa), sdesc_rows16(sa + BM * 16), idesc_s, 0u);
-                        }
-                        umma_commit(bar_accf(buf));
-                    }
+            for (int j = 0; j < 4; j++) {
+                const int ks = 4 * s + j;
+                const int kin = ks % T::G16;
+                const int g = ks / T::G16;
+                const int buf = g % T::kNacc;
+                if (kin == 0) {
+                    mbar_wait(bar_acce(buf), ((g / T::kNacc) & 1) ^ 1, abort_flag);
+                    tc_fence_after();
                 }
-                umma_commit(bar_empty(slot));
+                const uint32_t dcol = tmem_base + buf * T::kAccCols;
+                // +32 bytes per 16-element K slice: +2 in the descriptor's address field
+                if (elect_one()) umma_f16(dcol, ad0 + 2 * j, bd0 + 2 * j, idesc, kin != 0 ? 1u : 0u);
+                if (kin == T::G16 - 1 || ks == nk16 - 1) {
+                    if constexpr (T::kSB) {
+                        // S = wd (x) xd for this block: one bf16 MMA on the scale rows
+                        const uint32_t sa = sop_smem + slot * SmemLayout::sop_stage + (j >> 1) * SmemLayout::sop_block;
+                        const uint64_t sad = sdesc_rows16(sa), sbd = sdesc_rows16(sa + BM * 16);
+                        if (elect_one()) umma_f16(dcol + BN, sad, sbd, idesc_s, 0u);
+                    }
+                    if (elect_one()) umma_commit(bar_accf(buf));
+                }
             }
-            // every MMA and every commit-arrive of this CTA has landed once this barrier flips
-            umma_commit(bar_done);
-            mbar_wait_final(bar_done, 0);
+            if (elect_one()) umma_commit(bar_empty(slot));
+            __syncwarp();
         }
+        // every MMA and every commit-arrive of this CTA has landed once this barrier flips
+        if (elect_one()) umma_commit(bar_done);
+        __syncwarp();
+        mbar_wait_final(bar_done, 0);
         __syncwarp();
     } else {
         // =========================================================== epilogue

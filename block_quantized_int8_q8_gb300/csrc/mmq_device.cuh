@@ -62,13 +62,16 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Wait for the phase with the given parity to complete.  Bounded: returns false (and sets the
 // abort flag and the device error word) when the limit is exceeded or the CTA already aborted.
-// The abort flag and the clock are checked every 16 sleeps (each sleep is at most 0.2 ms).
+// The waiting thread polls with try_wait (which suspends it briefly in hardware between polls); a
+// long suspend-time hint is not used because the wake-up after the phase completes then lags by
+// hundreds of cycles on the pipeline's critical hand-offs.  The abort flag and the clock are checked
+// every 64 polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (int it = 1;; it++) {
-        if (mbar_try_wait_sleep(bar, parity)) return true;
-        if ((it & 15) != 0) continue;
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) != 0) continue;
         if (*abort_flag) return false;
         if (clock64() - t0 > MMQ_WAIT_LIMIT_CYCLES) {
             *abort_flag = 1;
@@ -98,6 +101,18 @@ __device__ __forceinline__ void fence_barrier_init() {
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One lane of a fully active warp returns true (the others false); the warp stays converged, so
+// values computed outside the elected region remain warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // ------------------------------------------------------------------------------------------ tcgen05
