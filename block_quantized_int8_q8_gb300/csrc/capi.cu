@@ -172,6 +172,24 @@ mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out, in
     if (!W || !Xq || !out) return MMQ_ERR_INVALID_ARG;
     if (!aligned16(W) || !aligned16(Xq) || !aligned16(out)) return MMQ_ERR_ALIGN;
     if (wtype == MMQ_W8A8 && (((M * K) & 3) || ((N * K) & 3))) return MMQ_ERR_ALIGN;
+    if (block_type(wtype) && tma_gemm_supported((int)wtype, K)) {
+        // the TMA-fed kernel (gemm_tma.cuh); the general kernel covers the remaining shapes
+        const Q81Layout L = q81_layout(M, K);
+        const uint8_t* xb = static_cast<const uint8_t*>(Xq);
+        TmaGemmArgs a{};
+        a.W = W;
+        a.xh = xb + L.h;
+        a.dT = reinterpret_cast<const float*>(xb + L.dT);
+        a.sT = reinterpret_cast<const float*>(xb + L.sT);
+        a.out = static_cast<float*>(out);
+        a.w_row_bytes = weight_row_bytes(wtype, K);
+        a.M = M;
+        a.N = N;
+        a.K = K;
+        a.Mp = L.Mp;
+        const cudaError_t e = run_gemm_tma((int)wtype, a, reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm");
+    }
     GemmParams p = dense_params(wtype, W, Xq, out, M, N, K);
     const cudaError_t e =
         dispatch(wtype, p, MODE_PROD, false, (int)((M + BN - 1) / BN), reinterpret_cast<cudaStream_t>(stream));
@@ -242,7 +260,7 @@ mmq_status mmq_read_device_errors(unsigned* bits, mmq_stream_t stream) {
     cudaError_t (*readers[])(unsigned*, cudaStream_t) = {read_clear_errors_quantize, read_clear_errors_route,
                                                          read_clear_errors_q8_0,     read_clear_errors_q4_0,
                                                          read_clear_errors_q4_k,     read_clear_errors_iq1_m,
-                                                         read_clear_errors_w8a8};
+                                                         read_clear_errors_w8a8,     read_clear_errors_tma};
     for (auto r : readers) {
         cudaError_t ei = r(bits, s);
         if (ei != cudaSuccess) e = ei;

@@ -1,0 +1,105 @@
+// gemm_tma.cu -- host side of the TMA-fed dense MMQ kernel (gemm_tma.cuh): tensor maps and launch.
+//
+// Four tensor maps per call, encoded on the host with the driver's cuTensorMapEncodeTiled (looked up
+// once through the runtime's driver entry-point query, so the library needs no -lcuda):
+//   raw  : the weight bytes as [N][row_bytes/16][16] uint8; box 128 rows x U units x 16 bytes (one
+//          raw super-stage); rows past N read as zeros.
+//   b    : the q8_1 shadow's fp16 codes [M][K]; box 128 tokens x 64 k, 128-byte swizzle (the MMA's
+//          K-major operand layout); tokens past M read as zeros.
+//   xd/xs: the block-major scales d^T, s^T [K/32][Mp]; box 2 blocks x 128 tokens.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+#include "gemm_tma.cuh"
+#include "internal.h"
+
+namespace mmq {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int WT>
+cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
+    using L = tma::Smem<WT>;
+    constexpr int U = tma::Geom<WT>::U;
+    CUtensorMap tm_raw, tm_b, tm_xd, tm_xs;
+    {
+        const cuuint64_t dims[3] = {16, (cuuint64_t)(a.w_row_bytes / 16), (cuuint64_t)a.N};
+        const cuuint64_t strides[2] = {16, (cuuint64_t)a.w_row_bytes};
+        const cuuint32_t box[3] = {16, (cuuint32_t)U, (cuuint32_t)BM};
+        if (!encode(&tm_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.W, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+        const cuuint32_t box[2] = {BK, BN};
+        if (!encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.xh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.M, (cuuint64_t)(a.K / 32)};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.Mp * 4};
+        const cuuint32_t box[2] = {BN, 2};
+        if (!encode(&tm_xd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dT, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        if (!encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.sT, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    auto kern = tma::mmq_gemm_tma_kernel<WT>;
+    static bool configured = false;       // per instantiation; the attribute is per function
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const dim3 grid((unsigned)((a.N + BM - 1) / BM), (unsigned)((a.M + BN - 1) / BN));
+    kern<<<grid, tma::NTHREADS, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N,
+                                                    (int)a.K);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tma_gemm_supported(int wt, long long K) {
+    if (wt == WT_IQ1_M) return K % 1024 == 0;
+    return (wt == WT_Q8_0 || wt == WT_Q4_0 || wt == WT_Q4_K) && K % 256 == 0;
+}
+
+cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s) {
+    switch (wt) {
+        case WT_Q8_0: return launch<WT_Q8_0>(a, s);
+        case WT_Q4_0: return launch<WT_Q4_0>(a, s);
+        case WT_Q4_K: return launch<WT_Q4_K>(a, s);
+        case WT_IQ1_M: return launch<WT_IQ1_M>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+MMQ_DEFINE_ERROR_READER(tma)
+
+}  // namespace mmq

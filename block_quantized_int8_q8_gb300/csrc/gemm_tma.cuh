@@ -1,0 +1,451 @@
+// gemm_tma.cuh -- the dense production MMQ kernel for the block types: TMA-fed, converter-group
+// pipelined, register rescale.
+//
+// Computes out[m,n] = sum_b wd[n,b] * xd[m,b] * I[m,n,b] (Q4_K: minus dmin*m_b*s[m,b]) with the exact
+// per-block integer dot I[m,n,b] = sum_{k in b} xq[m,k] * wq[n,k]  ("A Negative Result on int8
+// Tensor-Core MMQ", §2; "08 · R1 — int8 MMQ prefill GEMM", §2.1-§2.2 and §3.2).
+//
+// Pipeline of one CTA (128 weight rows x 128 tokens, all of K):
+//   * loader warp (one thread): TMA loads of (a) raw weight bytes, one "super-stage" of 256 k (IQ1_M:
+//     1024 k) for the 128 rows, into a two-slot raw ring; (b) the token operand, fp16 codes of the
+//     q8_1 shadow, 64 k x 128 tokens with the 128-byte swizzle straight into the MMA operand ring;
+//     (c) the tokens' block scales d (Q4_K also s) from the block-major shadow into a scale ring.
+//   * a converter group of four warps: each thread takes one weight row,
+//     reads its raw bytes from the raw ring (16-byte loads, conflict-free: the row pitch is an odd
+//     number of 16-byte units), unpacks them EXACTLY to fp16 integers (the same unpackers as the
+//     general kernel in gemm.cuh), stores the 128B-swizzled K-major operand row and the row's block
+//     scales.
+//   * MMA warp: two tcgen05.mma kind::f16 (M=128, N=128, K=16) per 32-k block into one of four
+//     128-column TMEM accumulators; a commit per block hands it to the epilogue.
+//   * eight epilogue warps: tcgen05.ld each finished block and apply acc += I * (xd * wd) in packed
+//     f32 pairs in registers ("A Negative Result", §2-§4: no shared-memory round trip of the
+//     accumulator).  IQ1_M's per-16 scale (2s+1) and Q4_K's 6-bit sub-block scale are folded into the
+//     integer operand (exact), so their block scale is the super-block d (IQ1_M: d/8).
+// Four accumulators decouple the tensor core from the epilogue by four blocks, so the rescale of block
+// b overlaps the MMAs of blocks b+1..b+3.
+#pragma once
+#include <cuda.h>
+#include "gemm.cuh"
+
+namespace mmq {
+namespace tma {
+
+constexpr int STAGES = 4;            // operand ring (A converted by the converters, B by TMA)
+constexpr int SC = 8;                // scale ring depth (converters run up to 4 stages ahead of the
+                                     // MMA, the epilogue trails it by up to 2)
+constexpr int RAW_SLOTS = 2;
+constexpr int NACC = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int GROUP_WARPS = 4;       // warps per converter group (one weight row per thread)
+constexpr int NGROUPS = 1;           // converter groups; group g converts the stages s = g (mod NGROUPS)
+constexpr int CONV_WARP0 = EPI_WARPS;
+constexpr int MMA_WARP = CONV_WARP0 + NGROUPS * GROUP_WARPS;
+constexpr int LOAD_WARP = MMA_WARP + 1;
+constexpr int NTHREADS = (LOAD_WARP + 1) * 32;
+constexpr long long ABORT_DRAIN_CYCLES = 2000000;   // ~1 ms: lets in-flight TMA writes land after an abort
+
+// Raw super-stage geometry: U 16-byte units per weight row, SS 64-k operand stages per super-stage.
+template <int WT> struct Geom;
+template <> struct Geom<WT_Q8_0> { static constexpr int U = 17, SS = 4; };    // 8 blocks x 34 B
+template <> struct Geom<WT_Q4_0> { static constexpr int U = 9, SS = 4; };     // 8 blocks x 18 B
+template <> struct Geom<WT_Q4_K> { static constexpr int U = 9, SS = 4; };     // one 144 B super-block
+template <> struct Geom<WT_IQ1_M> { static constexpr int U = 19, SS = 16; };  // four 76 B super-blocks
+
+template <int WT> struct Smem {
+    static constexpr bool kMin = WT == WT_Q4_K;               // Q4_K min term needs xs and wmn
+    static constexpr int a_off = 0;
+    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr int raw_slot = (BM * Geom<WT>::U * 16 + 1023) / 1024 * 1024;
+    static constexpr int raw_off = b_off + STAGES * B_STAGE_BYTES;
+    // one scale slot: xd[2][128] (TMA) | xs[2][128] (TMA, Q4_K) | wd[2][128] | wmn[2][128] (Q4_K)
+    static constexpr int xd_off = 0;
+    static constexpr int xs_off = 1024;
+    static constexpr int wd_off = kMin ? 2048 : 1024;
+    static constexpr int wmn_off = 3072;
+    static constexpr int sc_slot = kMin ? 4096 : 2048;
+    static constexpr int sc_off = raw_off + RAW_SLOTS * raw_slot;
+    static constexpr int bar_off = sc_off + SC * sc_slot;
+    static constexpr int n_bars = 2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NACC + 1;
+    static constexpr int misc_off = bar_off + n_bars * 8;
+    static constexpr int total = misc_off + 16;
+    static constexpr int alloc = total + 1024;                  // slack for 1024-byte alignment
+    static_assert(alloc <= 232448, "shared memory budget");
+};
+
+// ------------------------------------------------------------------------------------------ TMA
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------ raw reads
+// Copy NW consecutive 32-bit words starting at byte offset OFF of a raw row record (16-byte aligned
+// base) into r[DST..DST+NW), with whole 16-byte loads.
+template <int OFF, int NW, int DST>
+__device__ __forceinline__ void raw_words(uint32_t rrow, RawA& r) {
+    static_assert(OFF % 4 == 0, "word-aligned fields");
+    constexpr int c0 = OFF / 16, w0 = (OFF % 16) / 4, nch = (w0 + NW + 3) / 4;
+    uint32_t w[4 * nch];
+#pragma unroll
+    for (int c = 0; c < nch; c++) {
+        const uint4 v = ld_shared_u4(rrow + 16 * (c0 + c));
+        w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < NW; i++) r.w[DST + i] = w[w0 + i];
+}
+
+// The raw words of operand stage J of a super-stage, in the word order the unpackers expect.
+template <int WT, int J>
+__device__ __forceinline__ void load_raw(uint32_t rrow, RawA& r) {
+    if constexpr (WT == WT_Q8_0) {
+        raw_words<68 * J, 17, 0>(rrow, r);                     // blocks 2J, 2J+1
+    } else if constexpr (WT == WT_Q4_0) {
+        raw_words<36 * J, 9, 0>(rrow, r);
+    } else if constexpr (WT == WT_Q4_K) {
+        raw_words<0, 4, 0>(rrow, r);                           // d, dmin, 12 B of scales
+        raw_words<16 + 32 * J, 8, 4>(rrow, r);                 // codes of sub-blocks 2J, 2J+1
+    } else {
+        constexpr int sbk = J / 4, jj = J % 4;
+        raw_words<76 * sbk + 16 * jj, 4, 0>(rrow, r);          // 64 two-bit codes
+        raw_words<76 * sbk + 64, 3, 4>(rrow, r);               // signs, sub-scales, d
+    }
+}
+
+// ------------------------------------------------------------------------------------------ kernel
+struct Ctx {
+    uint32_t sb;             // shared-window address of the 1024-aligned tile base
+    uint32_t bar0;
+    volatile int* abort_flag;
+    int pt;                  // weight row within the tile (converters)
+    bool row_ok;
+    bool ok;
+};
+
+template <int WT> struct Bars {
+    __device__ static uint32_t full(const Ctx& c, int i) { return c.bar0 + 8u * i; }
+    __device__ static uint32_t empty(const Ctx& c, int i) { return c.bar0 + 8u * (STAGES + i); }
+    __device__ static uint32_t rfull(const Ctx& c, int i) { return c.bar0 + 8u * (2 * STAGES + i); }
+    __device__ static uint32_t rempty(const Ctx& c, int i) { return c.bar0 + 8u * (2 * STAGES + RAW_SLOTS + i); }
+    __device__ static uint32_t sfull(const Ctx& c, int i) { return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + i); }
+    __device__ static uint32_t sfree(const Ctx& c, int i) {
+        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + SC + i);
+    }
+    __device__ static uint32_t accf(const Ctx& c, int i) {
+        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + i);
+    }
+    __device__ static uint32_t acce(const Ctx& c, int i) {
+        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + NACC + i);
+    }
+    __device__ static uint32_t done(const Ctx& c) {
+        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NACC);
+    }
+};
+
+// Convert operand stage s = t*SS + J of raw super-stage t (this thread: weight row c.pt).
+template <int WT, int J>
+__device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t rrow) {
+    using L = Smem<WT>;
+    using B = Bars<WT>;
+    if (!c.ok) return;
+    const int s = t * Geom<WT>::SS + J;
+    const int slot = s & (STAGES - 1), ss = s % SC;
+    if (!mbar_wait_relaxed(B::empty(c, slot), ((s / STAGES) & 1) ^ 1, c.abort_flag) ||
+        !mbar_wait_relaxed(B::sfree(c, ss), ((s / SC) & 1) ^ 1, c.abort_flag)) {
+        c.ok = false;
+        return;
+    }
+    RawA r;
+    load_raw<WT, J>(rrow, r);
+    uint32_t h[32];
+    float wsc[2], wmn[2];
+    unpack_a<WT, true>(r, s, h, wsc, wmn);
+    if (!c.row_ok) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
+    const uint32_t at = c.sb + L::a_off + slot * A_STAGE_BYTES;
+#pragma unroll
+    for (int q = 0; q < 8; q++) st_shared_v4(at + sw128_off(c.pt, q), h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
+    st_shared_f32(scs + L::wd_off + 4 * c.pt, wsc[0]);
+    st_shared_f32(scs + L::wd_off + 4 * (BM + c.pt), wsc[1]);
+    if constexpr (L::kMin) {
+        st_shared_f32(scs + L::wmn_off + 4 * c.pt, wmn[0]);
+        st_shared_f32(scs + L::wmn_off + 4 * (BM + c.pt), wmn[1]);
+    }
+    fence_proxy_async_smem();        // the operand row -> tensor core
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        mbar_arrive(B::full(c, slot));
+        mbar_arrive(B::sfull(c, ss));
+    }
+}
+
+template <int WT, int GRP, int JJ, int NJJ>
+struct ConvUnroll {
+    __device__ static __forceinline__ void run(Ctx& c, int t, uint32_t rrow) {
+        convert_stage<WT, NGROUPS * JJ + GRP>(c, t, rrow);
+        ConvUnroll<WT, GRP, JJ + 1, NJJ>::run(c, t, rrow);
+    }
+};
+template <int WT, int GRP, int NJJ>
+struct ConvUnroll<WT, GRP, NJJ, NJJ> {
+    __device__ static __forceinline__ void run(Ctx&, int, uint32_t) {}
+};
+
+template <int WT, int GRP>
+__device__ __forceinline__ void converter_loop(Ctx& c, int nsuper) {
+    using L = Smem<WT>;
+    using B = Bars<WT>;
+    constexpr int U = Geom<WT>::U, SS = Geom<WT>::SS;
+    for (int t = 0; t < nsuper; t++) {
+        const int rs = t & 1;
+        if (!c.ok || !mbar_wait_relaxed(B::rfull(c, rs), (t >> 1) & 1, c.abort_flag)) {
+            c.ok = false;
+            return;
+        }
+        const uint32_t rrow = c.sb + L::raw_off + rs * L::raw_slot + c.pt * U * 16;
+        ConvUnroll<WT, GRP, 0, SS / NGROUPS>::run(c, t, rrow);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(B::rempty(c, rs));
+    }
+}
+
+// acc += I * (xd * wd) for one 16-column chunk qq of this thread's 64 columns (Q4_K also adds
+// -(dmin*m_b) * s[m,b]); xd and s are broadcast reads of the scale ring.
+template <bool MIN>
+__device__ __forceinline__ void rescale16(uint64_t (&acc2)[32], int qq, const uint32_t (&v)[16], uint32_t xdp,
+                                          uint32_t xsp, uint64_t w2, uint64_t nmn2) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; q4++) {
+        const float4 xd = ld_shared_f4(xdp + 64 * qq + 16 * q4);
+        const int a = 8 * qq + 2 * q4, j = 4 * q4;
+        acc2[a] = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), f2_mul(f2_pack(xd.x, xd.y), w2),
+                         acc2[a]);
+        acc2[a + 1] = f2_fma(f2_pack(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
+                             f2_mul(f2_pack(xd.z, xd.w), w2), acc2[a + 1]);
+        if constexpr (MIN) {
+            const float4 xs = ld_shared_f4(xsp + 64 * qq + 16 * q4);
+            acc2[a] = f2_fma(nmn2, f2_pack(xs.x, xs.y), acc2[a]);
+            acc2[a + 1] = f2_fma(nmn2, f2_pack(xs.z, xs.w), acc2[a + 1]);
+        }
+    }
+}
+
+template <int WT>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
+                        const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
+                        float* __restrict__ out, int M, int N, int K) {
+    using L = Smem<WT>;
+    using B = Bars<WT>;
+    constexpr int U = Geom<WT>::U, SS = Geom<WT>::SS;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+
+    Ctx c;
+    c.sb = smem_u32(smem);
+    c.bar0 = c.sb + L::bar_off;
+    c.abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+    c.pt = 0;
+    c.row_ok = true;
+    c.ok = true;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+
+    if (warp == MMA_WARP) {
+        if (lane == 0) {
+            for (int i = 0; i < STAGES; i++) {
+                mbar_init(B::full(c, i), GROUP_WARPS + 1);      // converter warps + the B load
+                mbar_init(B::empty(c, i), 1);
+            }
+            for (int i = 0; i < RAW_SLOTS; i++) {
+                mbar_init(B::rfull(c, i), 1);
+                mbar_init(B::rempty(c, i), NGROUPS * GROUP_WARPS);
+            }
+            for (int i = 0; i < SC; i++) {
+                mbar_init(B::sfull(c, i), GROUP_WARPS + 1);     // converter warps + the scale load
+                mbar_init(B::sfree(c, i), EPI_WARPS);
+            }
+            for (int i = 0; i < NACC; i++) {
+                mbar_init(B::accf(c, i), 1);
+                mbar_init(B::acce(c, i), EPI_WARPS);
+            }
+            mbar_init(B::done(c), 1);
+            *c.abort_flag = 0;
+            fence_barrier_init();
+        }
+        __syncwarp();
+        tmem_alloc(smem_u32(tmem_slot), NACC * BN);
+        tmem_relinquish();
+    } else if (warp == LOAD_WARP && lane == 0) {
+        tma_prefetch_desc(&tm_raw);
+        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_xd);
+        if constexpr (L::kMin) tma_prefetch_desc(&tm_xs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nstages = K / BK;
+
+    if (warp == LOAD_WARP) {
+        // =========================================================== TMA loader
+        if (lane == 0) {
+            for (int s = 0; s < nstages; s++) {
+                if (s % SS == 0) {
+                    const int t = s / SS, rs = t & 1;
+                    if (!mbar_wait_relaxed(B::rempty(c, rs), ((t >> 1) & 1) ^ 1, c.abort_flag)) break;
+                    mbar_arrive_expect_tx(B::rfull(c, rs), BM * U * 16);
+                    tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, t * U, n0, B::rfull(c, rs));
+                }
+                const int slot = s & (STAGES - 1);
+                if (!mbar_wait_relaxed(B::empty(c, slot), ((s / STAGES) & 1) ^ 1, c.abort_flag)) break;
+                mbar_arrive_expect_tx(B::full(c, slot), B_STAGE_BYTES);
+                tma_load_2d(c.sb + L::b_off + slot * B_STAGE_BYTES, &tm_b, BK * s, m0, B::full(c, slot));
+                const int ss = s % SC;
+                if (!mbar_wait_relaxed(B::sfree(c, ss), ((s / SC) & 1) ^ 1, c.abort_flag)) break;
+                const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
+                mbar_arrive_expect_tx(B::sfull(c, ss), L::kMin ? 2048u : 1024u);
+                tma_load_2d(scs + L::xd_off, &tm_xd, m0, 2 * s, B::sfull(c, ss));
+                if constexpr (L::kMin) tma_load_2d(scs + L::xs_off, &tm_xs, m0, 2 * s, B::sfull(c, ss));
+            }
+        }
+        __syncwarp();
+    } else if (warp >= CONV_WARP0 && warp < MMA_WARP) {
+        // =========================================================== converters
+        const int grp = (warp - CONV_WARP0) / GROUP_WARPS;
+        c.pt = ((warp - CONV_WARP0) % GROUP_WARPS) * 32 + lane;
+        c.row_ok = n0 + c.pt < N;
+        const int nsuper = nstages / SS;
+        if (grp == 0) converter_loop<WT, 0>(c, nsuper);
+        if constexpr (NGROUPS == 2) {
+            if (grp == 1) converter_loop<WT, NGROUPS - 1>(c, nsuper);
+        }
+    } else if (warp == MMA_WARP) {
+        // =========================================================== MMA issuer
+        const uint32_t idesc = idesc_f16_f32(BM, BN);
+        const uint32_t a_smem = c.sb + L::a_off;
+        const uint32_t b_smem = c.sb + L::b_off;
+        for (int s = 0; s < nstages; s++) {
+            if (*c.abort_flag) break;
+            const int slot = s & (STAGES - 1);
+            if (!mbar_wait(B::full(c, slot), (s / STAGES) & 1, c.abort_flag)) break;
+            tc_fence_after();
+            const uint64_t ad0 = sdesc_sw128(a_smem + slot * A_STAGE_BYTES);
+            const uint64_t bd0 = sdesc_sw128(b_smem + slot * B_STAGE_BYTES);
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int blk = 2 * s + (j >> 1), buf = blk & (NACC - 1);
+                if ((j & 1) == 0) {
+                    mbar_wait(B::acce(c, buf), ((blk / NACC) & 1) ^ 1, c.abort_flag);
+                    tc_fence_after();
+                }
+                // +32 bytes per 16-element K slice: +2 in the descriptor's address field
+                if (elect_one()) umma_f16(tmem_base + buf * BN, ad0 + 2 * j, bd0 + 2 * j, idesc, j & 1);
+                if (j & 1) {
+                    if (elect_one()) umma_commit(B::accf(c, buf));
+                }
+            }
+            if (elect_one()) umma_commit(B::empty(c, slot));
+            __syncwarp();
+        }
+        if (elect_one()) umma_commit(B::done(c));
+        __syncwarp();
+        mbar_wait_final(B::done(c), 0);
+        __syncwarp();
+    } else {
+        // =========================================================== epilogue
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int ch = warp >> 2;               // column half: tokens 64*ch .. 64*ch+63
+        const int r = 32 * q + lane;            // tile row (weight row n0 + r)
+        const int n = n0 + r;
+        const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + 64 * ch;
+        uint64_t acc2[32];                      // packed f32 pairs: columns 2t, 2t+1
+#pragma unroll
+        for (int j = 0; j < 32; j++) acc2[j] = 0ull;
+        const int nblocks = K / 32;
+        for (int b = 0; b < nblocks; b++) {
+            const int buf = b & (NACC - 1), s = b >> 1, i = b & 1, ss = s % SC;
+            if (i == 0 && !mbar_wait(B::sfull(c, ss), (s / SC) & 1, c.abort_flag)) break;
+            if (!mbar_wait(B::accf(c, buf), (b / NACC) & 1, c.abort_flag)) break;
+            tc_fence_after();
+            const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
+            const float wd = ld_shared_f32(scs + L::wd_off + 4 * (i * BM + r));
+            const uint64_t w2 = f2_pack(wd, wd);
+            uint64_t nmn2 = 0ull;
+            if constexpr (L::kMin) {
+                const float mn = ld_shared_f32(scs + L::wmn_off + 4 * (i * BM + r));
+                nmn2 = f2_pack(-mn, -mn);
+            }
+            const uint32_t xdp = scs + L::xd_off + 4 * (i * BN + 64 * ch);
+            const uint32_t xsp = scs + L::xs_off + 4 * (i * BN + 64 * ch);
+            const uint32_t tacc = tb + buf * BN;
+            // software pipeline over the four 16-column chunks: the TMEM load of chunk q+1 is in flight
+            // while chunk q is rescaled (tcgen05.wait::ld waits for every earlier load of the thread)
+            uint32_t va[16], vb[16];
+            tmem_ld16(tacc, va);
+            tmem_ld_wait(va);
+            tmem_ld16(tacc + 16, vb);
+            rescale16<L::kMin>(acc2, 0, va, xdp, xsp, w2, nmn2);
+            tmem_ld_wait(vb);
+            tmem_ld16(tacc + 32, va);
+            rescale16<L::kMin>(acc2, 1, vb, xdp, xsp, w2, nmn2);
+            tmem_ld_wait(va);
+            tmem_ld16(tacc + 48, vb);
+            rescale16<L::kMin>(acc2, 2, va, xdp, xsp, w2, nmn2);
+            tmem_ld_wait(vb);
+            tc_fence_before();              // every TMEM read of this accumulator is complete
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B::acce(c, buf));
+            rescale16<L::kMin>(acc2, 3, vb, xdp, xsp, w2, nmn2);
+            if (i == 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B::sfree(c, ss));
+            }
+        }
+        // ---- store: this thread's weight row n, tokens m0 + 64*ch + 0..63
+        if (n < N) {
+#pragma unroll
+            for (int t = 0; t < 32; t++) {
+                float a0, a1;
+                f2_unpack(acc2[t], a0, a1);
+                const int m = m0 + 64 * ch + 2 * t;
+                if (m < M) out[(long long)m * N + n] = a0;
+                if (m + 1 < M) out[(long long)(m + 1) * N + n] = a1;
+            }
+        }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (*c.abort_flag) {
+        // a wait gave up: give any TMA copy still in flight time to land before the CTA's shared
+        // memory is released
+        const long long t0 = clock64();
+        while (clock64() - t0 < ABORT_DRAIN_CYCLES) {
+        }
+    }
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem_base, NACC * BN);
+}
+
+}  // namespace tma
+}  // namespace mmq

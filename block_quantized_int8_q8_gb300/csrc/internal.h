@@ -8,16 +8,33 @@ struct GemmParams;
 
 // q8_1 buffer sections (byte offsets), see include/mmq.h
 struct Q81Layout {
-    long long ds, h, xs3, total;
+    long long ds, h, xs3, dT, sT, Mp, total;
 };
 inline Q81Layout q81_layout(long long M, long long K) {
     Q81Layout L;
+    const long long kb = K / 32;
+    L.Mp = (M + 3) / 4 * 4;                       // block-major rows padded to 16 bytes
     L.ds = M * K;
-    L.h = (M * K + M * (K / 32) * 8 + 255) / 256 * 256;
+    L.h = (M * K + M * kb * 8 + 255) / 256 * 256;
     L.xs3 = L.h + 2 * M * K;
-    L.total = (L.xs3 + M * (K / 32) * 16 + 255) / 256 * 256;
+    L.dT = (L.xs3 + M * kb * 16 + 255) / 256 * 256;
+    L.sT = L.dT + L.Mp * kb * 4;
+    L.total = (L.sT + L.Mp * kb * 4 + 255) / 256 * 256;
     return L;
 }
+
+// Arguments of the TMA-fed dense kernel (gemm_tma.cu).
+struct TmaGemmArgs {
+    const void* W;              // raw weights, N rows of w_row_bytes
+    const void* xh;             // q8_1 shadow: fp16 codes [M][K]
+    const float* dT;            // q8_1 shadow: d, block-major [K/32][Mp]
+    const float* sT;            // q8_1 shadow: s, block-major [K/32][Mp]
+    float* out;                 // f32 [M][N]
+    long long w_row_bytes;
+    long long M, N, K, Mp;
+};
+bool tma_gemm_supported(int wt, long long K);
+cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s);
 
 // Quantizer and shadow preparation (quantize.cu)
 cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq, cudaStream_t s);
@@ -52,6 +69,7 @@ cudaError_t read_clear_errors_q4_0(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_q4_k(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_iq1_m(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_w8a8(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_tma(unsigned* bits, cudaStream_t s);
 }  // namespace mmq
 
 // Defines read_clear_errors_<name> for the translation unit that expands it.

@@ -46,8 +46,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait with a suspend-time hint: a waiting thread sleeps in hardware until the phase completes
-// (or the hint expires) instead of spinning through issue slots other warps need.
+// try_wait with a suspend-time hint (1 us): a waiting thread sleeps in hardware until the phase
+// completes (or the hint expires) instead of spinning through issue slots other warps need.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -55,7 +55,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(200000u)
+        : "r"(bar), "r"(parity), "r"(1000u)
         : "memory");
     return ok != 0;
 }
@@ -72,6 +72,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     for (int it = 1;; it++) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) != 0) continue;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > MMQ_WAIT_LIMIT_CYCLES) {
+            *abort_flag = 1;
+            atomicOr(&g_mmq_device_errors, DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// The same bounded wait for threads off the critical path (producers that run ahead and wait for a
+// free slot): each poll may suspend the thread in hardware for up to ~1 us, leaving the issue slots to
+// the warps that do the work.
+__device__ __forceinline__ bool mbar_wait_relaxed(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (int it = 1;; it++) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if ((it & 15) != 0) continue;
         if (*abort_flag) return false;
         if (clock64() - t0 > MMQ_WAIT_LIMIT_CYCLES) {
             *abort_flag = 1;
@@ -199,6 +217,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The same wait, with the destination registers of the awaited load as in/out operands so that the
+// compiler cannot move their uses above it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
 
 // ------------------------------------------------------------------------------------------ fp16 packing
 // Exact small-integer -> fp16 conversion by exponent splicing: the fp16 pattern 0x6400 | b is

@@ -4,7 +4,8 @@
 // division), s = d * sum(q)  ("08 · R1 — int8 MMQ prefill GEMM", §2.2 q8_1 activation pipeline, and
 // the §3.2 reference quantizer; f32 scale, the block sum produced in the same pass).
 // Output layout (include/mmq.h): int8 q[M][K], float2 (d, s)[M][K/32], then the tensor-core shadow:
-// fp16 h[M][K] = q exactly, and bf16 {x1,x1,x2,x2,x3,x3,0,0} per block with x1 + x2 + x3 = d exactly.
+// fp16 h[M][K] = q exactly, bf16 {x1,x1,x2,x2,x3,x3,0,0} per block with x1 + x2 + x3 = d exactly,
+// and the block-major copies d^T, s^T [K/32][Mp] that the TMA-fed GEMM loads per 128-token tile.
 //
 // HBM-bound: 4 bytes read and 1.25 bytes written per value.  Eight lanes own one block (one float4
 // each); amax and sum(q) are warp-shuffle reductions over the eight lanes; every lane stores its
@@ -50,7 +51,9 @@ __device__ __forceinline__ int q8_code(float x, float d) {
 
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, uint32_t* __restrict__ q,
                                                            float2* __restrict__ ds, uint2* __restrict__ h,
-                                                           uint4* __restrict__ xs3, long long nblk) {
+                                                           uint4* __restrict__ xs3, float* __restrict__ dT,
+                                                           float* __restrict__ sT, int kb, long long Mp,
+                                                           long long nblk) {
     const int lane = threadIdx.x & 31, sub = lane & 7, grp = lane >> 3;
     const long long warp_id = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (gridDim.x * (long long)blockDim.x) >> 5;
@@ -86,8 +89,16 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
                                    ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
                 h[blk * 8 + sub] = codes_to_f16x4(q0, q1, q2, q3);
                 if (sub == 0) {
-                    ds[blk] = make_float2(d, __fmul_rn(d, (float)sum));
+                    const float sv = __fmul_rn(d, (float)sum);
+                    ds[blk] = make_float2(d, sv);
                     xs3[blk] = split3_record(d);
+                    const long long m = blk / kb, b = blk - m * kb;
+                    dT[b * Mp + m] = d;
+                    sT[b * Mp + m] = sv;
+                    for (long long mm = m + 1; mm < Mp && blk + kb >= nblk; mm++) {   // pad columns: zero
+                        dT[b * Mp + mm] = 0.f;
+                        sT[b * Mp + mm] = 0.f;
+                    }
                 }
             }
         }
@@ -108,21 +119,34 @@ cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq
     const Q81Layout L = q81_layout(M, K);
     quantize_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(
         reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(base), reinterpret_cast<float2*>(base + L.ds),
-        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3), nblk);
+        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3),
+        reinterpret_cast<float*>(base + L.dT), reinterpret_cast<float*>(base + L.sT), (int)(K / 32), L.Mp, nblk);
     return cudaGetLastError();
 }
 
 // Derived sections from existing q8_1 blocks: eight lanes per block, one 32-bit word of codes each.
 __global__ void __launch_bounds__(256) prepare_q8_1_kernel(const uint32_t* __restrict__ q,
                                                           const float2* __restrict__ ds, uint2* __restrict__ h,
-                                                          uint4* __restrict__ xs3, long long nblk) {
+                                                          uint4* __restrict__ xs3, float* __restrict__ dT,
+                                                          float* __restrict__ sT, int kb, long long Mp,
+                                                          long long nblk) {
     const long long stride = (gridDim.x * (long long)blockDim.x) >> 3;
     const int sub = threadIdx.x & 7;
     for (long long blk = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3; blk < nblk; blk += stride) {
         const uint32_t w = q[blk * 8 + sub];
         h[blk * 8 + sub] = codes_to_f16x4((int)(int8_t)(w & 0xff), (int)(int8_t)((w >> 8) & 0xff),
                                           (int)(int8_t)((w >> 16) & 0xff), (int)(int8_t)(w >> 24));
-        if (sub == 0) xs3[blk] = split3_record(ds[blk].x);
+        if (sub == 0) {
+            const float2 v = ds[blk];
+            xs3[blk] = split3_record(v.x);
+            const long long m = blk / kb, b = blk - m * kb;
+            dT[b * Mp + m] = v.x;
+            sT[b * Mp + m] = v.y;
+            for (long long mm = m + 1; mm < Mp && blk + kb >= nblk; mm++) {   // pad columns: zero
+                dT[b * Mp + mm] = 0.f;
+                sT[b * Mp + mm] = 0.f;
+            }
+        }
     }
 }
 
@@ -138,7 +162,8 @@ cudaError_t run_prepare_q8_1(void* xq, long long M, long long K, cudaStream_t s)
     const Q81Layout L = q81_layout(M, K);
     prepare_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(
         reinterpret_cast<const uint32_t*>(base), reinterpret_cast<const float2*>(base + L.ds),
-        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3), nblk);
+        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3),
+        reinterpret_cast<float*>(base + L.dT), reinterpret_cast<float*>(base + L.sT), (int)(K / 32), L.Mp, nblk);
     return cudaGetLastError();
 }
 

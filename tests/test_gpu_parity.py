@@ -55,17 +55,20 @@ def test_quantizer_bit_exact(M, K):
     assert np.array_equal(qg.cpu().numpy(), q)
     assert np.array_equal(dsg[..., 0].cpu().numpy().view(np.uint32), d.view(np.uint32))
     assert np.array_equal(dsg[..., 1].cpu().numpy().view(np.uint32), s.view(np.uint32))
-    _check_shadow(buf, q, d, M, K)
+    _check_shadow(buf, q, d, s, M, K)
 
 
-def _check_shadow(buf, q, d, M, K):
-    # derived sections: fp16 codes equal the int8 codes; the bf16 pieces sum exactly to d
-    h, xs3 = api.q8_1_shadow_views(buf, M, K)
+def _check_shadow(buf, q, d, s, M, K):
+    # derived sections: fp16 codes equal the int8 codes; the bf16 pieces sum exactly to d; the
+    # block-major copies are d and s transposed, bit for bit
+    h, xs3, dT, sT = api.q8_1_shadow_views(buf, M, K)
     assert np.array_equal(h.float().cpu().numpy(), q.astype(np.float32))
     pc = xs3.float().cpu().numpy().astype(np.float64)
     assert np.array_equal(pc[..., 0], pc[..., 1]) and np.array_equal(pc[..., 2], pc[..., 3])
     assert np.array_equal(pc[..., 4], pc[..., 5]) and np.all(pc[..., 6:] == 0)
     assert np.array_equal(pc[..., 0] + pc[..., 2] + pc[..., 4], d.astype(np.float64))
+    assert np.array_equal(dT.cpu().numpy().view(np.uint32), np.ascontiguousarray(d.T).view(np.uint32))
+    assert np.array_equal(sT.cpu().numpy().view(np.uint32), np.ascontiguousarray(s.T).view(np.uint32))
 
 
 def test_prepare_rebuilds_the_quantizer_shadow():
@@ -77,7 +80,7 @@ def test_prepare_rebuilds_the_quantizer_shadow():
     torch.cuda.synchronize()
     o = api.q8_1_offsets(M, K)
     assert torch.equal(buf[o["h"]:], packed[o["h"]:])
-    _check_shadow(packed, q, d, M, K)
+    _check_shadow(packed, q, d, s, M, K)
 
 
 def test_quantizer_extreme_scales_bit_exact():
