@@ -34,8 +34,11 @@ constexpr int STAGES = 4;            // operand ring (A converted by the convert
 constexpr int SC = 8;                // scale ring depth (converters run up to 4 stages ahead of the
                                      // MMA, the epilogue trails it by up to 2)
 constexpr int RAW_SLOTS = 2;
-constexpr int NACC = 4;
-constexpr int EPI_WARPS = 8;
+constexpr int NACC = 4;              // 128-column TMEM accumulators: two stage buffers of two blocks
+constexpr int NSB = NACC / 2;        // stage buffers handed between the MMA warp and the epilogue
+constexpr int EPI_WARPS = 16;         // four per TMEM lane quarter
+constexpr int EPI_COLS = BN * 4 / EPI_WARPS;   // tokens per epilogue thread (32)
+constexpr int EPI_CHUNKS = EPI_COLS / 16;      // 16-column TMEM loads per block
 constexpr int GROUP_WARPS = 4;       // warps per converter group (one weight row per thread)
 constexpr int NGROUPS = 1;           // converter groups; group g converts the stages s = g (mod NGROUPS)
 constexpr int CONV_WARP0 = EPI_WARPS;
@@ -65,7 +68,7 @@ template <int WT> struct Smem {
     static constexpr int sc_slot = kMin ? 4096 : 2048;
     static constexpr int sc_off = raw_off + RAW_SLOTS * raw_slot;
     static constexpr int bar_off = sc_off + SC * sc_slot;
-    static constexpr int n_bars = 2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NACC + 1;
+    static constexpr int n_bars = 2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NSB + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int total = misc_off + 16;
     static constexpr int alloc = total + 1024;                  // slack for 1024-byte alignment
@@ -151,10 +154,10 @@ template <int WT> struct Bars {
         return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + i);
     }
     __device__ static uint32_t acce(const Ctx& c, int i) {
-        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + NACC + i);
+        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + NSB + i);
     }
     __device__ static uint32_t done(const Ctx& c) {
-        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NACC);
+        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NSB);
     }
 };
 
@@ -225,10 +228,10 @@ __device__ __forceinline__ void converter_loop(Ctx& c, int nsuper) {
     }
 }
 
-// acc += I * (xd * wd) for one 16-column chunk qq of this thread's 64 columns (Q4_K also adds
+// acc += I * (xd * wd) for one 16-column chunk qq of this thread's columns (Q4_K also adds
 // -(dmin*m_b) * s[m,b]); xd and s are broadcast reads of the scale ring.
 template <bool MIN>
-__device__ __forceinline__ void rescale16(uint64_t (&acc2)[32], int qq, const uint32_t (&v)[16], uint32_t xdp,
+__device__ __forceinline__ void rescale16(uint64_t (&acc2)[EPI_COLS / 2], int qq, const uint32_t (&v)[16], uint32_t xdp,
                                           uint32_t xsp, uint64_t w2, uint64_t nmn2) {
 #pragma unroll
     for (int q4 = 0; q4 < 4; q4++) {
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mbar_init(B::sfull(c, i), GROUP_WARPS + 1);     // converter warps + the scale load
                 mbar_init(B::sfree(c, i), EPI_WARPS);
             }
-            for (int i = 0; i < NACC; i++) {
+            for (int i = 0; i < NSB; i++) {
                 mbar_init(B::accf(c, i), 1);
                 mbar_init(B::acce(c, i), EPI_WARPS);
             }
@@ -346,24 +349,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int s = 0; s < nstages; s++) {
             if (*c.abort_flag) break;
             const int slot = s & (STAGES - 1);
+            const int sb = s & (NSB - 1);      // stage buffer: accumulators 2*sb (block 2s), 2*sb+1 (block 2s+1)
             if (!mbar_wait(B::full(c, slot), (s / STAGES) & 1, c.abort_flag)) break;
+            mbar_wait(B::acce(c, sb), ((s / NSB) & 1) ^ 1, c.abort_flag);
             tc_fence_after();
             const uint64_t ad0 = sdesc_sw128(a_smem + slot * A_STAGE_BYTES);
             const uint64_t bd0 = sdesc_sw128(b_smem + slot * B_STAGE_BYTES);
 #pragma unroll
             for (int j = 0; j < 4; j++) {
-                const int blk = 2 * s + (j >> 1), buf = blk & (NACC - 1);
-                if ((j & 1) == 0) {
-                    mbar_wait(B::acce(c, buf), ((blk / NACC) & 1) ^ 1, c.abort_flag);
-                    tc_fence_after();
-                }
+                const int buf = 2 * sb + (j >> 1);
                 // +32 bytes per 16-element K slice: +2 in the descriptor's address field
                 if (elect_one()) umma_f16(tmem_base + buf * BN, ad0 + 2 * j, bd0 + 2 * j, idesc, j & 1);
-                if (j & 1) {
-                    if (elect_one()) umma_commit(B::accf(c, buf));
-                }
             }
-            if (elect_one()) umma_commit(B::empty(c, slot));
+            if (elect_one()) {
+                umma_commit(B::accf(c, sb));
+                umma_commit(B::empty(c, slot));
+            }
             __syncwarp();
         }
         if (elect_one()) umma_commit(B::done(c));
@@ -373,60 +374,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         // =========================================================== epilogue
         const int q = warp & 3;                 // TMEM lane quarter
-        const int ch = warp >> 2;               // column half: tokens 64*ch .. 64*ch+63
+        const int cq = warp >> 2;               // column group: tokens EPI_COLS*cq ..
         const int r = 32 * q + lane;            // tile row (weight row n0 + r)
         const int n = n0 + r;
-        const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + 64 * ch;
-        uint64_t acc2[32];                      // packed f32 pairs: columns 2t, 2t+1
+        const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + EPI_COLS * cq;
+        uint64_t acc2[EPI_COLS / 2];            // packed f32 pairs: columns 2t, 2t+1
 #pragma unroll
-        for (int j = 0; j < 32; j++) acc2[j] = 0ull;
-        const int nblocks = K / 32;
-        for (int b = 0; b < nblocks; b++) {
-            const int buf = b & (NACC - 1), s = b >> 1, i = b & 1, ss = s % SC;
-            if (i == 0 && !mbar_wait(B::sfull(c, ss), (s / SC) & 1, c.abort_flag)) break;
-            if (!mbar_wait(B::accf(c, buf), (b / NACC) & 1, c.abort_flag)) break;
+        for (int j = 0; j < EPI_COLS / 2; j++) acc2[j] = 0ull;
+        for (int s = 0; s < nstages; s++) {
+            const int sb = s & (NSB - 1), ss = s % SC;
+            if (!mbar_wait(B::sfull(c, ss), (s / SC) & 1, c.abort_flag)) break;
+            if (!mbar_wait(B::accf(c, sb), (s / NSB) & 1, c.abort_flag)) break;
             tc_fence_after();
             const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
-            const float wd = ld_shared_f32(scs + L::wd_off + 4 * (i * BM + r));
-            const uint64_t w2 = f2_pack(wd, wd);
-            uint64_t nmn2 = 0ull;
-            if constexpr (L::kMin) {
-                const float mn = ld_shared_f32(scs + L::wmn_off + 4 * (i * BM + r));
-                nmn2 = f2_pack(-mn, -mn);
+            uint64_t w2[2], nmn2[2] = {0ull, 0ull};
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const float wd = ld_shared_f32(scs + L::wd_off + 4 * (i * BM + r));
+                w2[i] = f2_pack(wd, wd);
+                if constexpr (L::kMin) {
+                    const float mn = ld_shared_f32(scs + L::wmn_off + 4 * (i * BM + r));
+                    nmn2[i] = f2_pack(-mn, -mn);
+                }
             }
-            const uint32_t xdp = scs + L::xd_off + 4 * (i * BN + 64 * ch);
-            const uint32_t xsp = scs + L::xs_off + 4 * (i * BN + 64 * ch);
-            const uint32_t tacc = tb + buf * BN;
-            // software pipeline over the four 16-column chunks: the TMEM load of chunk q+1 is in flight
-            // while chunk q is rescaled (tcgen05.wait::ld waits for every earlier load of the thread)
+            // the stage's two blocks as 2*EPI_CHUNKS 16-column chunks in one software pipeline: the TMEM
+            // load of chunk k+1 is in flight while chunk k is rescaled
+            constexpr int TC = 2 * EPI_CHUNKS;
+            const uint32_t tacc = tb + 2 * sb * BN;
             uint32_t va[16], vb[16];
             tmem_ld16(tacc, va);
             tmem_ld_wait(va);
-            tmem_ld16(tacc + 16, vb);
-            rescale16<L::kMin>(acc2, 0, va, xdp, xsp, w2, nmn2);
-            tmem_ld_wait(vb);
-            tmem_ld16(tacc + 32, va);
-            rescale16<L::kMin>(acc2, 1, vb, xdp, xsp, w2, nmn2);
-            tmem_ld_wait(va);
-            tmem_ld16(tacc + 48, vb);
-            rescale16<L::kMin>(acc2, 2, va, xdp, xsp, w2, nmn2);
-            tmem_ld_wait(vb);
-            tc_fence_before();              // every TMEM read of this accumulator is complete
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B::acce(c, buf));
-            rescale16<L::kMin>(acc2, 3, vb, xdp, xsp, w2, nmn2);
-            if (i == 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B::sfree(c, ss));
+#pragma unroll
+            for (int k = 0; k < TC; k++) {
+                const int i = k / EPI_CHUNKS, qq = k % EPI_CHUNKS;          // block of the stage, chunk
+                const int kn = k + 1, in = kn / EPI_CHUNKS, qn = kn % EPI_CHUNKS;
+                uint32_t(&cur)[16] = (k & 1) ? vb : va;
+                uint32_t(&nxt)[16] = (k & 1) ? va : vb;
+                if (kn < TC) tmem_ld16(tacc + in * BN + 16 * qn, nxt);
+                rescale16<L::kMin>(acc2, qq, cur, scs + L::xd_off + 4 * (i * BN + EPI_COLS * cq),
+                                   scs + L::xs_off + 4 * (i * BN + EPI_COLS * cq), w2[i], nmn2[i]);
+                if (kn < TC) tmem_ld_wait(nxt);
+                if (kn + 1 == TC) {
+                    tc_fence_before();          // every TMEM read of this stage buffer is complete
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B::acce(c, sb));
+                }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B::sfree(c, ss));
         }
-        // ---- store: this thread's weight row n, tokens m0 + 64*ch + 0..63
+        // ---- store: this thread's weight row n, tokens m0 + EPI_COLS*cq + 0..EPI_COLS-1
         if (n < N) {
 #pragma unroll
-            for (int t = 0; t < 32; t++) {
+            for (int t = 0; t < EPI_COLS / 2; t++) {
                 float a0, a1;
                 f2_unpack(acc2[t], a0, a1);
-                const int m = m0 + 64 * ch + 2 * t;
+                const int m = m0 + EPI_COLS * cq + 2 * t;
                 if (m < M) out[(long long)m * N + n] = a0;
                 if (m + 1 < M) out[(long long)(m + 1) * N + n] = a1;
             }
