@@ -228,23 +228,22 @@ __device__ __forceinline__ void converter_loop(Ctx& c, int nsuper) {
     }
 }
 
-// acc += I * (xd * wd) for one 16-column chunk qq of this thread's columns (Q4_K also adds
-// -(dmin*m_b) * s[m,b]); xd and s are broadcast reads of the scale ring.
+// acc += I * (xd * wd) (Q4_K also -(dmin*m_b) * s[m,b]) for one 16-lane half of a warp's TMEM
+// quarter, in the 16x256b fragment layout: v[4j + 2e + c] is row 8e + t/4 of the half, column
+// 8j + 2(t%4) + c of the warp's 32 columns.  xd2[j] / xs2[j] hold the two column scales of group j,
+// w[e] / mn[e] the row scales.
 template <bool MIN>
-__device__ __forceinline__ void rescale16(uint64_t (&acc2)[EPI_COLS / 2], int qq, const uint32_t (&v)[16], uint32_t xdp,
-                                          uint32_t xsp, uint64_t w2, uint64_t nmn2) {
+__device__ __forceinline__ void rescale_half(uint64_t (&acc2)[8], const uint32_t (&v)[16], const uint64_t (&xd2)[4],
+                                             const uint64_t (&xs2)[4], const float (&w)[2], const float (&mn)[2]) {
 #pragma unroll
-    for (int q4 = 0; q4 < 4; q4++) {
-        const float4 xd = ld_shared_f4(xdp + 64 * qq + 16 * q4);
-        const int a = 8 * qq + 2 * q4, j = 4 * q4;
-        acc2[a] = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), f2_mul(f2_pack(xd.x, xd.y), w2),
-                         acc2[a]);
-        acc2[a + 1] = f2_fma(f2_pack(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
-                             f2_mul(f2_pack(xd.z, xd.w), w2), acc2[a + 1]);
-        if constexpr (MIN) {
-            const float4 xs = ld_shared_f4(xsp + 64 * qq + 16 * q4);
-            acc2[a] = f2_fma(nmn2, f2_pack(xs.x, xs.y), acc2[a]);
-            acc2[a + 1] = f2_fma(nmn2, f2_pack(xs.z, xs.w), acc2[a + 1]);
+    for (int e = 0; e < 2; e++) {
+        const uint64_t w2 = f2_pack(w[e], w[e]);
+        const uint64_t nmn2 = f2_pack(-mn[e], -mn[e]);
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            const int a = 4 * e + jj, r = 4 * jj + 2 * e;
+            acc2[a] = f2_fma(f2_pack(__uint_as_float(v[r]), __uint_as_float(v[r + 1])), f2_mul(xd2[jj], w2), acc2[a]);
+            if constexpr (MIN) acc2[a] = f2_fma(nmn2, xs2[jj], acc2[a]);
         }
     }
 }
@@ -373,48 +372,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
     } else {
         // =========================================================== epilogue
-        const int q = warp & 3;                 // TMEM lane quarter
-        const int cq = warp >> 2;               // column group: tokens EPI_COLS*cq ..
-        const int r = 32 * q + lane;            // tile row (weight row n0 + r)
-        const int n = n0 + r;
+        // Each warp owns TMEM lane quarter q (weight rows 32q..32q+31) and tokens 32cq..32cq+31, read in
+        // the 16x256b fragment layout: per 16-lane half h, thread t holds rows 16h + 8e + t/4 (e = 0, 1)
+        // and tokens 8j + 2(t%4) + {0, 1} (j = 0..3).  A thread thus needs 4 row scales and 8 token
+        // scales per block (two-lane-group loads, no whole-warp broadcast of the token scales).
+        const int q = warp & 3;
+        const int cq = warp >> 2;
+        const int tq = lane >> 2, tc = lane & 3;
         const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + EPI_COLS * cq;
-        uint64_t acc2[EPI_COLS / 2];            // packed f32 pairs: columns 2t, 2t+1
+        uint64_t acc[2][8];                     // [half][4e + j]: packed f32 pair, tokens 8j + 2tc + {0, 1}
 #pragma unroll
-        for (int j = 0; j < EPI_COLS / 2; j++) acc2[j] = 0ull;
+        for (int h = 0; h < 2; h++)
+#pragma unroll
+            for (int a = 0; a < 8; a++) acc[h][a] = 0ull;
         for (int s = 0; s < nstages; s++) {
             const int sb = s & (NSB - 1), ss = s % SC;
             if (!mbar_wait(B::sfull(c, ss), (s / SC) & 1, c.abort_flag)) break;
             if (!mbar_wait(B::accf(c, sb), (s / NSB) & 1, c.abort_flag)) break;
             tc_fence_after();
             const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
-            uint64_t w2[2], nmn2[2] = {0ull, 0ull};
-#pragma unroll
-            for (int i = 0; i < 2; i++) {
-                const float wd = ld_shared_f32(scs + L::wd_off + 4 * (i * BM + r));
-                w2[i] = f2_pack(wd, wd);
-                if constexpr (L::kMin) {
-                    const float mn = ld_shared_f32(scs + L::wmn_off + 4 * (i * BM + r));
-                    nmn2[i] = f2_pack(-mn, -mn);
-                }
-            }
-            // the stage's two blocks as 2*EPI_CHUNKS 16-column chunks in one software pipeline: the TMEM
-            // load of chunk k+1 is in flight while chunk k is rescaled
-            constexpr int TC = 2 * EPI_CHUNKS;
             const uint32_t tacc = tb + 2 * sb * BN;
+            // four chunks (block i, half h) in one software pipeline: the TMEM load of chunk k+1 is in
+            // flight while chunk k is rescaled
             uint32_t va[16], vb[16];
-            tmem_ld16(tacc, va);
+            tmem_ld_16x256b_x4(tacc, va);
             tmem_ld_wait(va);
+            uint64_t xd2[4], xs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int k = 0; k < TC; k++) {
-                const int i = k / EPI_CHUNKS, qq = k % EPI_CHUNKS;          // block of the stage, chunk
-                const int kn = k + 1, in = kn / EPI_CHUNKS, qn = kn % EPI_CHUNKS;
+            for (int k = 0; k < 4; k++) {
+                const int i = k >> 1, h = k & 1;                       // block of the stage, lane half
+                const int kn = k + 1;
                 uint32_t(&cur)[16] = (k & 1) ? vb : va;
                 uint32_t(&nxt)[16] = (k & 1) ? va : vb;
-                if (kn < TC) tmem_ld16(tacc + in * BN + 16 * qn, nxt);
-                rescale16<L::kMin>(acc2, qq, cur, scs + L::xd_off + 4 * (i * BN + EPI_COLS * cq),
-                                   scs + L::xs_off + 4 * (i * BN + EPI_COLS * cq), w2[i], nmn2[i]);
-                if (kn < TC) tmem_ld_wait(nxt);
-                if (kn + 1 == TC) {
+                if (kn < 4) tmem_ld_16x256b_x4(tacc + (kn >> 1) * BN + ((uint32_t)(16 * (kn & 1)) << 16), nxt);
+                if (h == 0) {                                          // token scales of block i
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj++) {
+                        const uint32_t col = EPI_COLS * cq + 8 * jj + 2 * tc;
+                        const float2 x = ld_shared_f2(scs + L::xd_off + 4 * (i * BN + col));
+                        xd2[jj] = f2_pack(x.x, x.y);
+                        if constexpr (L::kMin) {
+                            const float2 y = ld_shared_f2(scs + L::xs_off + 4 * (i * BN + col));
+                            xs2[jj] = f2_pack(y.x, y.y);
+                        }
+                    }
+                }
+                float w[2], mn[2] = {0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 2; e++) {
+                    const int row = 32 * q + 16 * h + 8 * e + tq;
+                    w[e] = ld_shared_f32(scs + L::wd_off + 4 * (i * BM + row));
+                    if constexpr (L::kMin) mn[e] = ld_shared_f32(scs + L::wmn_off + 4 * (i * BM + row));
+                }
+                rescale_half<L::kMin>(acc[h], cur, xd2, xs2, w, mn);
+                if (kn < 4) tmem_ld_wait(nxt);
+                if (kn == 3) {
                     tc_fence_before();          // every TMEM read of this stage buffer is complete
                     __syncwarp();
                     if (lane == 0) mbar_arrive(B::acce(c, sb));
@@ -423,15 +435,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(B::sfree(c, ss));
         }
-        // ---- store: this thread's weight row n, tokens m0 + EPI_COLS*cq + 0..EPI_COLS-1
-        if (n < N) {
+        // ---- store: rows n0 + 32q + 16h + 8e + tq, tokens m0 + 32cq + 8j + 2tc + {0, 1}
 #pragma unroll
-            for (int t = 0; t < EPI_COLS / 2; t++) {
-                float a0, a1;
-                f2_unpack(acc2[t], a0, a1);
-                const int m = m0 + EPI_COLS * cq + 2 * t;
-                if (m < M) out[(long long)m * N + n] = a0;
-                if (m + 1 < M) out[(long long)(m + 1) * N + n] = a1;
+        for (int h = 0; h < 2; h++) {
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int n = n0 + 32 * q + 16 * h + 8 * e + tq;
+                if (n >= N) continue;
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++) {
+                    float a0, a1;
+                    f2_unpack(acc[h][4 * e + jj], a0, a1);
+                    const int m = m0 + EPI_COLS * cq + 8 * jj + 2 * tc;
+                    if (m < M) out[(long long)m * N + n] = a0;
+                    if (m + 1 < M) out[(long long)(m + 1) * N + n] = a1;
+                }
             }
         }
     }
