@@ -174,6 +174,23 @@ __device__ __forceinline__ void u8x4_to_f16x4(uint32_t u, uint32_t bias_f16x2, u
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias_f16x2));
 }
 
+// fp16x2 bits of two floats (round to nearest; the callers pass exactly representable values).
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Keep bits 8-9 of each 16-bit half (a 2-bit code placed there by a byte permute) and add the fp16
+// exponent of 1024: the halves become 1024 + 256*code exactly.
+__device__ __forceinline__ uint32_t lop_or_magic(uint32_t x) {
+    return (x & 0x03000300u) | 0x64006400u;
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t field_le(const uint32_t* words, int pos, int width) {
     const int wi = pos >> 5, off = pos & 31;
     const uint32_t v = __funnelshift_r(words[wi], words[wi + 1], off);
@@ -238,6 +255,11 @@ __device__ __forceinline__ void unpack_a(const RawA& r, int s, uint32_t (&h)[32]
             }
         }
     } else if constexpr (WT == WT_IQ1_M) {
+        // operand value v = mult * (8g + sigma), g = code - 1, mult = 2s+1 (production fold) or 1.
+        // Two codes of one sign group at a time: a byte permute puts them at bits 8-9 of the two halves
+        // of an fp16x2 word, OR-ing in the exponent gives 1024 + 256*code exactly, and one fp16 FMA
+        // maps that to mult*(8*code - 8 + sigma) = (1024 + 256*code) * (mult/32) + mult*(sigma - 40).
+        // Every intermediate is an integer (or mult/32) well inside fp16's exact range.
         const int j = s & 3;
         const uint32_t signs = (r.w[4] >> (8 * j)) & 0xFFu;    // one bit per 8 values of this stage
         const uint32_t sbits[3] = {(r.w[5] >> 0), r.w[6] & 0xFFFFu, 0u};   // bytes 68..73 of the block
@@ -246,18 +268,27 @@ __device__ __forceinline__ void unpack_a(const RawA& r, int s, uint32_t (&h)[32]
         wmn[0] = wmn[1] = 0.f;
 #pragma unroll
         for (int q = 0; q < 4; q++) {                          // 16-value sub-scale groups
-            const int mult = PROD_FOLD ? (int)(2u * field_le(sbits, 3 * (4 * j + q), 3) + 1u) : 1;
-            const uint32_t cw = r.w[q];                        // 16 two-bit codes
+            const float mult = PROD_FOLD ? (float)(2u * field_le(sbits, 3 * (4 * j + q), 3) + 1u) : 1.f;
+            const uint32_t cw = r.w[q];                        // 16 two-bit codes, value 4i+t at byte i
+            const uint32_t c0 = cw & 0x03030303u;              // codes 4i
+            const uint32_t c1 = (cw >> 2) & 0x03030303u;       // codes 4i+1
+            const uint32_t c2 = (cw >> 4) & 0x03030303u;       // codes 4i+2
+            const uint32_t c3 = (cw >> 6) & 0x03030303u;       // codes 4i+3
+            const uint32_t a2 = f2_to_h2(mult * 0.03125f, mult * 0.03125f);
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                const int k = 16 * q + e;
-                const int sg0 = ((signs >> (k >> 3)) & 1u) ? -1 : 1;
-                const int g0 = (int)((cw >> (2 * e)) & 3u) - 1;
-                const int g1 = (int)((cw >> (2 * e + 2)) & 3u) - 1;
-                const int v0 = mult * (8 * g0 + sg0);
-                const int v1 = mult * (8 * g1 + sg0);          // e, e+1 share the 8-value sign group
-                const uint32_t pair = (uint32_t)(v0 + 256) | ((uint32_t)(v1 + 256) << 16);
-                h[k >> 1] = u10x2_to_f16x2(pair, 0x65006500u);   // minus (1024 + 256)
+            for (int hf = 0; hf < 2; hf++) {                   // sign groups: values 8hf..8hf+7 of the 16
+                const float sig = ((signs >> (2 * q + hf)) & 1u) ? -1.f : 1.f;
+                const float bc = mult * (sig - 40.f);
+                const uint32_t b2 = f2_to_h2(bc, bc);
+#pragma unroll
+                for (int ii = 0; ii < 2; ii++) {
+                    const int i = 2 * hf + ii;                 // byte of the word: values 4i..4i+3
+                    const uint32_t sel = (uint32_t)(i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12));
+                    const uint32_t p01 = lop_or_magic(__byte_perm(c0, c1, sel));
+                    const uint32_t p23 = lop_or_magic(__byte_perm(c2, c3, sel));
+                    h[8 * q + 2 * i] = hfma2_u32(p01, a2, b2);
+                    h[8 * q + 2 * i + 1] = hfma2_u32(p23, a2, b2);
+                }
             }
         }
     } else {                                                    // W8A8
