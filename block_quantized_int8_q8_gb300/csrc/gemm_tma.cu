@@ -42,6 +42,19 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, 
     return r == CUDA_SUCCESS;
 }
 
+// Multiprocessor count of the current device (looked up once per device).
+int sm_count() {
+    static int counts[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 template <int WT>
 cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     using L = tma::Smem<WT>;
@@ -77,9 +90,28 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const dim3 grid((unsigned)((a.N + BM - 1) / BM), (unsigned)((a.M + BN - 1) / BN));
-    kern<<<grid, tma::NTHREADS, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N,
-                                                    (int)a.K);
+    // Tail split: when the last wave of whole tiles would leave at least half the SMs idle, the last
+    // token-tile rows are computed as two K halves each (twice the CTAs at half the time); their output
+    // rows are zeroed first and both halves add into them.
+    const long long ntn = (a.N + BM - 1) / BM, ntm = (a.M + BN - 1) / BN, T = ntn * ntm;
+    const int sms = sm_count();
+    const long long nst = a.K / BK;
+    long long split_rows = 0;
+    if (sms > 0 && T > sms && nst % (2 * tma::Geom<WT>::SS) == 0) {
+        const long long r = T - (T - 1) / sms * sms;          // tiles in the last wave
+        if (2 * r <= sms) split_rows = (r + ntn - 1) / ntn;
+        if (split_rows >= ntm) split_rows = 0;
+    }
+    const long long nfull = T - split_rows * ntn;
+    if (split_rows > 0) {
+        const long long m_begin = (ntm - split_rows) * BN;
+        const cudaError_t e = cudaMemsetAsync(a.out + m_begin * a.N, 0, (size_t)((a.M - m_begin) * a.N) * sizeof(float),
+                                              stream);
+        if (e != cudaSuccess) return e;
+    }
+    const dim3 grid((unsigned)(nfull + 2 * split_rows * ntn));
+    kern<<<grid, tma::NTHREADS, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K,
+                                                    (int)ntn, (int)nfull);
     return cudaGetLastError();
 }
 

@@ -178,6 +178,8 @@ __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t rrow) {
     load_raw<WT, J>(rrow, r);
     uint32_t h[32];
     float wsc[2], wmn[2];
+    // the unpackers use only s % 4 (the stage's place in a 256-value super-block); K ranges start on
+    // super-stage boundaries, so the local index gives the same value and keeps it a compile-time one
     unpack_a<WT, true>(r, s, h, wsc, wmn);
     if (!c.row_ok) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
     const uint32_t at = c.sb + L::a_off + slot * A_STAGE_BYTES;
@@ -252,14 +254,24 @@ template <int WT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
-                        float* __restrict__ out, int M, int N, int K) {
+                        float* __restrict__ out, int M, int N, int K, int ntn, int nfull) {
     using L = Smem<WT>;
     using B = Bars<WT>;
     constexpr int U = Geom<WT>::U, SS = Geom<WT>::SS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+    // Tile of this CTA (weight-row tiles fastest).  CTAs past the first nfull take the remaining tiles
+    // in pairs: each pair splits its tile's K range in two halves and both add into a zeroed output
+    // (two addends onto zero: the f32 result does not depend on their order).
+    int tile = blockIdx.x, part = -1;
+    if (tile >= nfull) {
+        tile = nfull + ((tile - nfull) >> 1);
+        part = (blockIdx.x - nfull) & 1;
+    }
+    const int n0 = (tile % ntn) * BM, m0 = (tile / ntn) * BN;
+    const int nstages = part < 0 ? K / BK : K / BK / 2;       // stages of this CTA's K range
+    const int s0 = part < 0 ? 0 : part * nstages;
 
     Ctx c;
     c.sb = smem_u32(smem);
@@ -305,7 +317,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int nstages = K / BK;
 
     if (warp == LOAD_WARP) {
         // =========================================================== TMA loader
@@ -315,18 +326,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int t = s / SS, rs = t & 1;
                     if (!mbar_wait_relaxed(B::rempty(c, rs), ((t >> 1) & 1) ^ 1, c.abort_flag)) break;
                     mbar_arrive_expect_tx(B::rfull(c, rs), BM * U * 16);
-                    tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, t * U, n0, B::rfull(c, rs));
+                    tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * U, n0,
+                                B::rfull(c, rs));
                 }
                 const int slot = s & (STAGES - 1);
                 if (!mbar_wait_relaxed(B::empty(c, slot), ((s / STAGES) & 1) ^ 1, c.abort_flag)) break;
                 mbar_arrive_expect_tx(B::full(c, slot), B_STAGE_BYTES);
-                tma_load_2d(c.sb + L::b_off + slot * B_STAGE_BYTES, &tm_b, BK * s, m0, B::full(c, slot));
+                tma_load_2d(c.sb + L::b_off + slot * B_STAGE_BYTES, &tm_b, BK * (s + s0), m0, B::full(c, slot));
                 const int ss = s % SC;
                 if (!mbar_wait_relaxed(B::sfree(c, ss), ((s / SC) & 1) ^ 1, c.abort_flag)) break;
                 const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
                 mbar_arrive_expect_tx(B::sfull(c, ss), L::kMin ? 2048u : 1024u);
-                tma_load_2d(scs + L::xd_off, &tm_xd, m0, 2 * s, B::sfull(c, ss));
-                if constexpr (L::kMin) tma_load_2d(scs + L::xs_off, &tm_xs, m0, 2 * s, B::sfull(c, ss));
+                tma_load_2d(scs + L::xd_off, &tm_xd, m0, 2 * (s + s0), B::sfull(c, ss));
+                if constexpr (L::kMin) tma_load_2d(scs + L::xs_off, &tm_xs, m0, 2 * (s + s0), B::sfull(c, ss));
             }
         }
         __syncwarp();
@@ -447,8 +459,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float a0, a1;
                     f2_unpack(acc[h][4 * e + jj], a0, a1);
                     const int m = m0 + EPI_COLS * cq + 8 * jj + 2 * tc;
-                    if (m < M) out[(long long)m * N + n] = a0;
-                    if (m + 1 < M) out[(long long)(m + 1) * N + n] = a1;
+                    if (part < 0) {
+                        if (m < M) out[(long long)m * N + n] = a0;
+                        if (m + 1 < M) out[(long long)(m + 1) * N + n] = a1;
+                    } else {
+                        if (m < M) atomicAdd(out + (long long)m * N + n, a0);
+                        if (m + 1 < M) atomicAdd(out + (long long)(m + 1) * N + n, a1);
+                    }
                 }
             }
         }
