@@ -110,7 +110,7 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     const dim3 grid((unsigned)(nfull + 2 * split_rows * ntn));
-    kern<<<grid, tma::NTHREADS, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K,
+    kern<<<grid, tma::Warps<WT>::kThreads, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K,
                                                     (int)ntn, (int)nfull);
     return cudaGetLastError();
 }

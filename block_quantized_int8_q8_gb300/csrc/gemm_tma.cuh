@@ -10,7 +10,7 @@
 //     1024 k) for the 128 rows, into a two-slot raw ring; (b) the token operand, fp16 codes of the
 //     q8_1 shadow, 64 k x 128 tokens with the 128-byte swizzle straight into the MMA operand ring;
 //     (c) the tokens' block scales d (Q4_K also s) from the block-major shadow into a scale ring.
-//   * a converter group of four warps: each thread takes one weight row,
+//   * a converter group (two warps, four for IQ1_M): each thread takes two weight rows (one for IQ1_M),
 //     reads its raw bytes from the raw ring (16-byte loads, conflict-free: the row pitch is an odd
 //     number of 16-byte units), unpacks them EXACTLY to fp16 integers (the same unpackers as the
 //     general kernel in gemm.cuh), stores the 128B-swizzled K-major operand row and the row's block
@@ -39,12 +39,18 @@ constexpr int NSB = NACC / 2;        // stage buffers handed between the MMA war
 constexpr int EPI_WARPS = 16;         // four per TMEM lane quarter
 constexpr int EPI_COLS = BN * 4 / EPI_WARPS;   // tokens per epilogue thread (32)
 constexpr int EPI_CHUNKS = EPI_COLS / 16;      // 16-column TMEM loads per block
-constexpr int GROUP_WARPS = 4;       // warps per converter group (one weight row per thread)
-constexpr int NGROUPS = 1;           // converter groups; group g converts the stages s = g (mod NGROUPS)
-constexpr int CONV_WARP0 = EPI_WARPS;
-constexpr int MMA_WARP = CONV_WARP0 + NGROUPS * GROUP_WARPS;
-constexpr int LOAD_WARP = MMA_WARP + 1;
-constexpr int NTHREADS = (LOAD_WARP + 1) * 32;
+// Warp roles per weight type: 16 epilogue warps, the converter warps, the MMA warp, the TMA loader warp.
+// Two converter warps (two weight rows per thread) keep up with the rescale for Q8_0 / Q4_0 / Q4_K and
+// leave 96 registers per thread (20 warps); IQ1_M's unpack is the heaviest per row and gets four (22
+// warps, 80 registers).
+template <int WT> struct Warps {
+    static constexpr int kConv = (WT == WT_IQ1_M) ? 4 : 2;
+    static constexpr int kRowsPerConv = BM / (kConv * 32);
+    static constexpr int kConv0 = EPI_WARPS;
+    static constexpr int kMma = kConv0 + kConv;
+    static constexpr int kLoad = kMma + 1;
+    static constexpr int kThreads = (kLoad + 1) * 32;
+};
 constexpr long long ABORT_DRAIN_CYCLES = 2000000;   // ~1 ms: lets in-flight TMA writes land after an abort
 
 // Raw super-stage geometry: U 16-byte units per weight row, SS 64-k operand stages per super-stage.
@@ -136,8 +142,8 @@ struct Ctx {
     uint32_t sb;             // shared-window address of the 1024-aligned tile base
     uint32_t bar0;
     volatile int* abort_flag;
-    int pt;                  // weight row within the tile (converters)
-    bool row_ok;
+    int pt;                  // first weight row of this converter thread (rows pt + 32*kConv*i)
+    int rows_valid;          // weight rows of the tile below N
     bool ok;
 };
 
@@ -161,9 +167,9 @@ template <int WT> struct Bars {
     }
 };
 
-// Convert operand stage s = t*SS + J of raw super-stage t (this thread: weight row c.pt).
+// Convert operand stage s = t*SS + J of raw super-stage t (this thread: weight rows c.pt + 64*i).
 template <int WT, int J>
-__device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t rrow) {
+__device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t raw) {
     using L = Smem<WT>;
     using B = Bars<WT>;
     if (!c.ok) return;
@@ -174,23 +180,28 @@ __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t rrow) {
         c.ok = false;
         return;
     }
-    RawA r;
-    load_raw<WT, J>(rrow, r);
-    uint32_t h[32];
-    float wsc[2], wmn[2];
-    // the unpackers use only s % 4 (the stage's place in a 256-value super-block); K ranges start on
-    // super-stage boundaries, so the local index gives the same value and keeps it a compile-time one
-    unpack_a<WT, true>(r, s, h, wsc, wmn);
-    if (!c.row_ok) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
     const uint32_t at = c.sb + L::a_off + slot * A_STAGE_BYTES;
-#pragma unroll
-    for (int q = 0; q < 8; q++) st_shared_v4(at + sw128_off(c.pt, q), h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
     const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
-    st_shared_f32(scs + L::wd_off + 4 * c.pt, wsc[0]);
-    st_shared_f32(scs + L::wd_off + 4 * (BM + c.pt), wsc[1]);
-    if constexpr (L::kMin) {
-        st_shared_f32(scs + L::wmn_off + 4 * c.pt, wmn[0]);
-        st_shared_f32(scs + L::wmn_off + 4 * (BM + c.pt), wmn[1]);
+#pragma unroll 1
+    for (int rr = 0; rr < Warps<WT>::kRowsPerConv; rr++) {
+        const int row = c.pt + rr * Warps<WT>::kConv * 32;
+        RawA r;
+        load_raw<WT, J>(raw + row * Geom<WT>::U * 16, r);
+        uint32_t h[32];
+        float wsc[2], wmn[2];
+        // the unpackers use only s % 4 (the stage's place in a 256-value super-block); K ranges start on
+        // super-stage boundaries, so the local index gives the same value and keeps it a compile-time one
+        unpack_a<WT, true>(r, s, h, wsc, wmn);
+        if (row >= c.rows_valid) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+            st_shared_v4(at + sw128_off(row, q), h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        st_shared_f32(scs + L::wd_off + 4 * row, wsc[0]);
+        st_shared_f32(scs + L::wd_off + 4 * (BM + row), wsc[1]);
+        if constexpr (L::kMin) {
+            st_shared_f32(scs + L::wmn_off + 4 * row, wmn[0]);
+            st_shared_f32(scs + L::wmn_off + 4 * (BM + row), wmn[1]);
+        }
     }
     fence_proxy_async_smem();        // the operand row -> tensor core
     __syncwarp();
@@ -200,31 +211,30 @@ __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t rrow) {
     }
 }
 
-template <int WT, int GRP, int JJ, int NJJ>
+template <int WT, int J, int NJ>
 struct ConvUnroll {
     __device__ static __forceinline__ void run(Ctx& c, int t, uint32_t rrow) {
-        convert_stage<WT, NGROUPS * JJ + GRP>(c, t, rrow);
-        ConvUnroll<WT, GRP, JJ + 1, NJJ>::run(c, t, rrow);
+        convert_stage<WT, J>(c, t, rrow);
+        ConvUnroll<WT, J + 1, NJ>::run(c, t, rrow);
     }
 };
-template <int WT, int GRP, int NJJ>
-struct ConvUnroll<WT, GRP, NJJ, NJJ> {
+template <int WT, int NJ>
+struct ConvUnroll<WT, NJ, NJ> {
     __device__ static __forceinline__ void run(Ctx&, int, uint32_t) {}
 };
 
-template <int WT, int GRP>
+template <int WT>
 __device__ __forceinline__ void converter_loop(Ctx& c, int nsuper) {
     using L = Smem<WT>;
     using B = Bars<WT>;
-    constexpr int U = Geom<WT>::U, SS = Geom<WT>::SS;
+    constexpr int SS = Geom<WT>::SS;
     for (int t = 0; t < nsuper; t++) {
         const int rs = t & 1;
         if (!c.ok || !mbar_wait_relaxed(B::rfull(c, rs), (t >> 1) & 1, c.abort_flag)) {
             c.ok = false;
             return;
         }
-        const uint32_t rrow = c.sb + L::raw_off + rs * L::raw_slot + c.pt * U * 16;
-        ConvUnroll<WT, GRP, 0, SS / NGROUPS>::run(c, t, rrow);
+        ConvUnroll<WT, 0, SS>::run(c, t, c.sb + L::raw_off + rs * L::raw_slot);
         __syncwarp();
         if ((threadIdx.x & 31) == 0) mbar_arrive(B::rempty(c, rs));
     }
@@ -251,7 +261,7 @@ __device__ __forceinline__ void rescale_half(uint64_t (&acc2)[8], const uint32_t
 }
 
 template <int WT>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
                         float* __restrict__ out, int M, int N, int K, int ntn, int nfull) {
@@ -278,22 +288,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     c.bar0 = c.sb + L::bar_off;
     c.abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
     c.pt = 0;
-    c.row_ok = true;
+    c.rows_valid = N - n0;
     c.ok = true;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
 
-    if (warp == MMA_WARP) {
+    if (warp == Warps<WT>::kMma) {
         if (lane == 0) {
             for (int i = 0; i < STAGES; i++) {
-                mbar_init(B::full(c, i), GROUP_WARPS + 1);      // converter warps + the B load
+                mbar_init(B::full(c, i), Warps<WT>::kConv + 1);     // converter warps + the B load
                 mbar_init(B::empty(c, i), 1);
             }
             for (int i = 0; i < RAW_SLOTS; i++) {
                 mbar_init(B::rfull(c, i), 1);
-                mbar_init(B::rempty(c, i), NGROUPS * GROUP_WARPS);
+                mbar_init(B::rempty(c, i), Warps<WT>::kConv);
             }
             for (int i = 0; i < SC; i++) {
-                mbar_init(B::sfull(c, i), GROUP_WARPS + 1);     // converter warps + the scale load
+                mbar_init(B::sfull(c, i), Warps<WT>::kConv + 1);    // converter warps + the scale load
                 mbar_init(B::sfree(c, i), EPI_WARPS);
             }
             for (int i = 0; i < NSB; i++) {
@@ -307,7 +317,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
         tmem_alloc(smem_u32(tmem_slot), NACC * BN);
         tmem_relinquish();
-    } else if (warp == LOAD_WARP && lane == 0) {
+    } else if (warp == Warps<WT>::kLoad && lane == 0) {
         tma_prefetch_desc(&tm_raw);
         tma_prefetch_desc(&tm_b);
         tma_prefetch_desc(&tm_xd);
@@ -318,7 +328,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == LOAD_WARP) {
+    if (warp == Warps<WT>::kLoad) {
         // =========================================================== TMA loader
         if (lane == 0) {
             for (int s = 0; s < nstages; s++) {
@@ -342,17 +352,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= CONV_WARP0 && warp < MMA_WARP) {
+    } else if (warp >= Warps<WT>::kConv0 && warp < Warps<WT>::kMma) {
         // =========================================================== converters
-        const int grp = (warp - CONV_WARP0) / GROUP_WARPS;
-        c.pt = ((warp - CONV_WARP0) % GROUP_WARPS) * 32 + lane;
-        c.row_ok = n0 + c.pt < N;
-        const int nsuper = nstages / SS;
-        if (grp == 0) converter_loop<WT, 0>(c, nsuper);
-        if constexpr (NGROUPS == 2) {
-            if (grp == 1) converter_loop<WT, NGROUPS - 1>(c, nsuper);
-        }
-    } else if (warp == MMA_WARP) {
+        c.pt = (warp - Warps<WT>::kConv0) * 32 + lane;
+        converter_loop<WT>(c, nstages / SS);
+    } else if (warp == Warps<WT>::kMma) {
         // =========================================================== MMA issuer
         const uint32_t idesc = idesc_f16_f32(BM, BN);
         const uint32_t a_smem = c.sb + L::a_off;
@@ -482,7 +486,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     tc_fence_after();
-    if (warp == MMA_WARP) tmem_dealloc(tmem_base, NACC * BN);
+    if (warp == Warps<WT>::kMma) tmem_dealloc(tmem_base, NACC * BN);
 }
 
 }  // namespace tma
