@@ -190,6 +190,10 @@ mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out, in
         const cudaError_t e = run_gemm_tma((int)wtype, a, reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm");
     }
+    if (wtype == MMQ_W8A8) {
+        const cudaError_t e = run_gemm_w8a8_tma(W, Xq, out, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm");
+    }
     GemmParams p = dense_params(wtype, W, Xq, out, M, N, K);
     const cudaError_t e =
         dispatch(wtype, p, MODE_PROD, false, (int)((M + BN - 1) / BN), reinterpret_cast<cudaStream_t>(stream));

@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <mutex>
 #include "gemm_tma.cuh"
+#include "gemm_w8a8_tma.cuh"
 #include "internal.h"
 
 namespace mmq {
@@ -115,7 +116,35 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Raw int8 rows [rows][K]; box 128 rows x 64 bytes (one 64-k stage) with the 64-byte swizzle.
+bool encode_int8_rows(CUtensorMap* m, const void* base, long long rows, long long K) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K};
+    const cuuint32_t box[2] = {64, 128};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 }  // namespace
+
+cudaError_t run_gemm_w8a8_tma(const void* W, const void* X, void* out, long long M, long long N, long long K,
+                              cudaStream_t stream) {
+    CUtensorMap tm_w, tm_x;
+    if (!encode_int8_rows(&tm_w, W, N, K) || !encode_int8_rows(&tm_x, X, M, K)) return cudaErrorInvalidValue;
+    const float* ws = reinterpret_cast<const float*>(static_cast<const uint8_t*>(W) + N * K);
+    const float* xs = reinterpret_cast<const float*>(static_cast<const uint8_t*>(X) + M * K);
+    auto kern = w8tma::mmq_w8a8_tma_kernel;
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, w8tma::Smem::alloc);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const long long tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
+    kern<<<(unsigned)tiles, w8tma::NTHREADS, w8tma::Smem::alloc, stream>>>(
+        tm_w, tm_x, ws, xs, static_cast<__nv_bfloat16*>(out), (int)M, (int)N, (int)K);
+    return cudaGetLastError();
+}
 
 bool tma_gemm_supported(int wt, long long K) {
     if (wt == WT_IQ1_M) return K % 1024 == 0;

@@ -35,6 +35,10 @@ struct TmaGemmArgs {
 };
 bool tma_gemm_supported(int wt, long long K);
 cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s);
+// Per-channel W8A8 on the TMA-fed kernel (gemm_w8a8_tma.cuh): W = int8 [N][K] + f32 ws[N],
+// X = int8 [M][K] + f32 xs[M], out bf16 [M][N]; K % 64 == 0.
+cudaError_t run_gemm_w8a8_tma(const void* W, const void* X, void* out, long long M, long long N, long long K,
+                              cudaStream_t s);
 
 // Quantizer and shadow preparation (quantize.cu)
 cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq, cudaStream_t s);
