@@ -2,8 +2,9 @@
 //
 // Four tensor maps per call, encoded on the host with the driver's cuTensorMapEncodeTiled (looked up
 // once through the runtime's driver entry-point query, so the library needs no -lcuda):
-//   raw  : the weight bytes as [N][row_bytes/16][16] uint8; box 128 rows x U units x 16 bytes (one
-//          raw super-stage); rows past N read as zeros.
+//   raw  : the weight bytes [N][row_bytes] uint8; box 128 rows x U*16 bytes (one raw super-stage) as a
+//          2-D box when it fits a box dimension (Q4_0, Q4_K), else as [N][row_bytes/16][16] with a
+//          3-D box of U 16-byte units (Q8_0, IQ1_M); rows past N read as zeros.
 //   b    : the q8_1 shadow's fp16 codes [M][K]; box 128 tokens x 64 k, 128-byte swizzle (the MMA's
 //          K-major operand layout); tokens past M read as zeros.
 //   xd/xs: the block-major scales d^T, s^T [K/32][Mp]; box 2 blocks x 128 tokens.
@@ -62,11 +63,19 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     constexpr int U = tma::Geom<WT>::U;
     CUtensorMap tm_raw, tm_b, tm_xd, tm_xs;
     {
-        const cuuint64_t dims[3] = {16, (cuuint64_t)(a.w_row_bytes / 16), (cuuint64_t)a.N};
-        const cuuint64_t strides[2] = {16, (cuuint64_t)a.w_row_bytes};
-        const cuuint32_t box[3] = {16, (cuuint32_t)U, (cuuint32_t)BM};
-        if (!encode(&tm_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.W, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
+        if (U * 16 <= 256) {                  // one 2-D box of whole row chunks (fewer TMA requests)
+            const cuuint64_t dims[2] = {(cuuint64_t)a.w_row_bytes, (cuuint64_t)a.N};
+            const cuuint64_t strides[1] = {(cuuint64_t)a.w_row_bytes};
+            const cuuint32_t box[2] = {(cuuint32_t)(U * 16), (cuuint32_t)BM};
+            if (!encode(&tm_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.W, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+                return cudaErrorInvalidValue;
+        } else {                              // rows wider than a box dimension: 16-byte units
+            const cuuint64_t dims[3] = {16, (cuuint64_t)(a.w_row_bytes / 16), (cuuint64_t)a.N};
+            const cuuint64_t strides[2] = {16, (cuuint64_t)a.w_row_bytes};
+            const cuuint32_t box[3] = {16, (cuuint32_t)U, (cuuint32_t)BM};
+            if (!encode(&tm_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.W, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+                return cudaErrorInvalidValue;
+        }
     }
     {
         const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};

@@ -336,8 +336,12 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
                     const int t = s / SS, rs = t & 1;
                     if (!mbar_wait_relaxed(B::rempty(c, rs), ((t >> 1) & 1) ^ 1, c.abort_flag)) break;
                     mbar_arrive_expect_tx(B::rfull(c, rs), BM * U * 16);
-                    tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * U, n0,
-                                B::rfull(c, rs));
+                    if constexpr (U * 16 <= 256)
+                        tma_load_2d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, (t + s0 / SS) * U * 16, n0,
+                                    B::rfull(c, rs));
+                    else
+                        tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * U, n0,
+                                    B::rfull(c, rs));
                 }
                 const int slot = s & (STAGES - 1);
                 if (!mbar_wait_relaxed(B::empty(c, slot), ((s / STAGES) & 1) ^ 1, c.abort_flag)) break;
