@@ -39,6 +39,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ------------------------------------------------------------------------------------------ helpers
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (1 rank: x).  The job's time is its slowest replica's."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step: float, world: int, steps: int, seconds: float) -> float:
+    """Whole-job rate: every rank processes units_per_step per step (weak scaling), over the slowest
+    rank's time."""
+    return units_per_step * world * steps / seconds
+
+
 def workload_ops(name: str) -> tuple[float, int]:
     """(2*M*N*K of the whole step, tokens per step); MoE counts every (token, slot) row."""
     w = synth.WORKLOADS[name]
@@ -352,11 +369,7 @@ def main():
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K_steps)]
     gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K_steps)]
     quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K_steps)]
-    dev_total = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([dev_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_total = float(t.item())
+    dev_total = max_over_ranks(sum(step_ms) / 1e3, dev)
     errs = api.read_device_errors()
 
     # ---------------------------------------------------------------- end to end through the C ABI
@@ -382,12 +395,8 @@ def main():
             host_out.copy_(out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_s = e0.elapsed_time(e1) / 1e3
-        if world > 1:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": ops * world * args.e2e_steps / e2e_s / 1e12, "unit": "TOPS",
+        e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+        e2e = {"value": job_throughput(ops, world, args.e2e_steps, e2e_s) / 1e12, "unit": "TOPS",
                "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
                "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
                "steps": args.e2e_steps, "note": "weights resident in HBM; activations in, outputs out"}
@@ -419,13 +428,13 @@ def main():
     except OSError:
         pass
 
-    value = ops * world * K_steps / dev_total / 1e12
+    value = job_throughput(ops, world, K_steps, dev_total) / 1e12
     line = {"metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": K_steps,
             "warmup": args.warmup, "ms_per_step": dev_total / K_steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "s8 x s8 -> exact block dot (fp16 tensor cores, f32 accumulate), f32 rescale",
             "data": "synthetic", "config": workload_config(name),
-            "tok_per_s": tokens * world * K_steps / dev_total,
+            "tok_per_s": job_throughput(tokens, world, K_steps, dev_total),
             "pct_int8_peak": (100.0 * value / world / int8_peak) if int8_peak else None,
             "int8_peak_tops": int8_peak,
             "int8_peak_source": "measured live: mma.sync.m16n8k32.s8, the only int8 tensor path on sm_103a",
