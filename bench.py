@@ -406,10 +406,10 @@ def main():
     gemm_avg = statistics.mean(gemm_ms) / 1e3
     achieved = ops / gemm_avg / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    # the dense block-type GEMM runs the TMA-fed kernel (IQ1_M when K % 1024 == 0); MoE, W8A8 and the
-    # remaining shapes run the general kernel
+    # the dense block-type GEMM runs the TMA-fed kernel (IQ1_M when K % 1024 == 0), W8A8 its own
+    # TMA-fed kernel; MoE and the remaining shapes run the general kernel
     tma_path = (not is_moe) and wt != synth.W8A8 and (wt != synth.IQ1_M or K % 1024 == 0)
-    kernel = "mmq_gemm_tma_kernel" if tma_path else "mmq_gemm_kernel"
+    kernel = "mmq_w8a8_tma_kernel" if wt == synth.W8A8 else ("mmq_gemm_tma_kernel" if tma_path else "mmq_gemm_kernel")
     roofline = {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(name),
                 "peak_source": f"{peak_src} dense bf16 burst (fp16 operands, same nominal rate)",
