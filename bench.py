@@ -315,7 +315,7 @@ def main():
         if is_moe:
             ids = torch.from_numpy(pb.ids).to(dev)
             out = torch.empty((M, pb.ids.shape[1], N), dtype=torch.float32, device=dev)
-            ws = torch.empty(api.gemm_id_workspace_bytes(M, pb.ids.shape[1], pb.experts), dtype=torch.uint8,
+            ws = torch.empty(api.gemm_id_workspace_bytes(M, K, pb.ids.shape[1], pb.experts), dtype=torch.uint8,
                              device=dev)
             launches_per_step = 6           # quantize, 4 routing kernels, grouped GEMM
         else:

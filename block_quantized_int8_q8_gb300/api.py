@@ -60,7 +60,7 @@ def load():
     lib.mmq_quantize_q8_1.restype = I
     lib.mmq_gemm.argtypes = [I, P, P, P, I64, I64, I64, P]
     lib.mmq_gemm.restype = I
-    lib.mmq_gemm_id_workspace_bytes.argtypes = [I64, I, I]
+    lib.mmq_gemm_id_workspace_bytes.argtypes = [I64, I64, I, I]
     lib.mmq_gemm_id_workspace_bytes.restype = SZ
     lib.mmq_gemm_id.argtypes = [I, P, I, P, P, I, P, I64, I64, I64, P, SZ, P]
     lib.mmq_gemm_id.restype = I
@@ -108,8 +108,8 @@ def w8a8_act_bytes(M: int, K: int) -> int:
     return int(load().mmq_w8a8_act_bytes(M, K))
 
 
-def gemm_id_workspace_bytes(M: int, slots: int, experts: int) -> int:
-    return int(load().mmq_gemm_id_workspace_bytes(M, slots, experts))
+def gemm_id_workspace_bytes(M: int, K: int, slots: int, experts: int) -> int:
+    return int(load().mmq_gemm_id_workspace_bytes(M, K, slots, experts))
 
 
 def q8_1_offsets(M: int, K: int) -> dict:
@@ -195,7 +195,7 @@ def gemm_id(wtype: int, W: torch.Tensor, n_experts: int, Xq: torch.Tensor, ids: 
     slots = ids.shape[1]
     if out is None:
         out = torch.empty((M, slots, N), dtype=torch.float32, device=W.device)
-    need = gemm_id_workspace_bytes(M, slots, n_experts)
+    need = gemm_id_workspace_bytes(M, K, slots, n_experts)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=W.device)
     _check(load().mmq_gemm_id(wtype, _ptr(W), n_experts, _ptr(Xq), _ptr(ids), slots, _ptr(out), M, N, K,

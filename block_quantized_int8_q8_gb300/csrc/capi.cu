@@ -85,15 +85,19 @@ GemmParams dense_params(mmq_type t, const void* W, const void* Xq, void* out, lo
     return p;
 }
 
+// mmq_gemm_id workspace: the routing lists, then the gathered MoE operand of the TMA-fed kernel
+// (fp16 codes [Rg][K], block-major d and s [K/32][Rg], each work item's rows at a 4-aligned offset).
 struct IdLayout {
-    size_t counts, offsets, cursor, nwork, work, rowlist, total;
+    size_t counts, offsets, cursor, nwork, work, rowlist, gstart, xg, dTg, sTg, total;
+    long long Rg;
     int max_work;
 };
 
-IdLayout id_layout(long long M, int slots, int E) {
+IdLayout id_layout(long long M, long long K, int slots, int E) {
     IdLayout L{};
     const long long rows = M * slots;
     L.max_work = (int)((rows + BN - 1) / BN + E);
+    L.Rg = (rows + 3ll * L.max_work + 3) / 4 * 4;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -106,6 +110,10 @@ IdLayout id_layout(long long M, int slots, int E) {
     L.nwork = take(sizeof(int));
     L.work = take(sizeof(int) * 3 * (size_t)L.max_work);
     L.rowlist = take(sizeof(int) * (size_t)rows);
+    L.gstart = take(sizeof(int) * (size_t)L.max_work);
+    L.xg = take((size_t)L.Rg * (size_t)K * 2);
+    L.dTg = take((size_t)(K / 32) * (size_t)L.Rg * 4);
+    L.sTg = take((size_t)(K / 32) * (size_t)L.Rg * 4);
     L.total = off;
     return L;
 }
@@ -215,9 +223,9 @@ mmq_status mmq_gemm_debug_partials(mmq_type wtype, const void* W, const void* Xq
     return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm_debug_partials");
 }
 
-size_t mmq_gemm_id_workspace_bytes(int64_t M, int n_slots, int n_experts) {
-    if (M < 0 || n_slots <= 0 || n_experts <= 0) return 0;
-    return id_layout(M, n_slots, n_experts).total;
+size_t mmq_gemm_id_workspace_bytes(int64_t M, int64_t K, int n_slots, int n_experts) {
+    if (M < 0 || K < 0 || n_slots <= 0 || n_experts <= 0) return 0;
+    return id_layout(M, K, n_slots, n_experts).total;
 }
 
 mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void* Xq, const int32_t* expert_ids,
@@ -232,7 +240,7 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
     if (M == 0 || N == 0) return MMQ_OK;
     if (!W || !Xq || !expert_ids || !out) return MMQ_ERR_INVALID_ARG;
     if (!aligned16(W) || !aligned16(Xq) || !aligned16(out) || !aligned16(expert_ids)) return MMQ_ERR_ALIGN;
-    const IdLayout L = id_layout(M, n_slots, n_experts);
+    const IdLayout L = id_layout(M, K, n_slots, n_experts);
     if (!workspace || workspace_bytes < L.total) return MMQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MMQ_ERR_ALIGN;
     uint8_t* wb = static_cast<uint8_t*>(workspace);
@@ -247,6 +255,48 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "mmq_gemm_id routing");
+    if (tma_gemm_supported((int)wtype, K) && (long long)n_experts * N < (1ll << 31) && L.Rg < (1ll << 31)) {
+        // TMA-fed kernel: gather each work item's token rows, then one CTA per (item, weight-row tile)
+        const Q81Layout X = q81_layout(M, K);
+        const uint8_t* xb = static_cast<const uint8_t*>(Xq);
+        MoeGatherArgs g{};
+        g.work = ws.work;
+        g.nwork = ws.nwork;
+        g.rowlist = ws.rowlist;
+        g.slots = n_slots;
+        g.max_work = L.max_work;
+        g.xh = xb + X.h;
+        g.dT = reinterpret_cast<const float*>(xb + X.dT);
+        g.sT = reinterpret_cast<const float*>(xb + X.sT);
+        g.Mp = X.Mp;
+        g.K = K;
+        g.gstart = reinterpret_cast<int*>(wb + L.gstart);
+        g.xg = wb + L.xg;
+        g.dTg = reinterpret_cast<float*>(wb + L.dTg);
+        g.sTg = reinterpret_cast<float*>(wb + L.sTg);
+        g.Rg = L.Rg;
+        e = run_moe_gather(g, s);
+        if (e != cudaSuccess) return cuda_fail(e, "mmq_gemm_id gather");
+        TmaGemmArgs a;
+        a.W = W;
+        a.xh = g.xg;
+        a.dT = g.dTg;
+        a.sT = g.sTg;
+        a.out = out;
+        a.w_row_bytes = weight_row_bytes(wtype, K);
+        a.M = L.Rg;
+        a.N = N;
+        a.K = K;
+        a.Mp = L.Rg;
+        a.E = n_experts;
+        a.work = ws.work;
+        a.nwork = ws.nwork;
+        a.gstart = g.gstart;
+        a.rowlist = ws.rowlist;
+        a.max_work = L.max_work;
+        e = run_gemm_tma((int)wtype, a, s);
+        return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm_id");
+    }
     GemmParams p = dense_params(wtype, W, Xq, out, M, N, K);
     p.rowlist = ws.rowlist;
     p.work = ws.work;

@@ -62,15 +62,16 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     using L = tma::Smem<WT>;
     constexpr int U = tma::Geom<WT>::U;
     CUtensorMap tm_raw, tm_b, tm_xd, tm_xs;
+    const long long wrows = a.E * a.N;      // MoE: every expert's rows, back to back
     {
         if (U * 16 <= 256) {                  // one 2-D box of whole row chunks (fewer TMA requests)
-            const cuuint64_t dims[2] = {(cuuint64_t)a.w_row_bytes, (cuuint64_t)a.N};
+            const cuuint64_t dims[2] = {(cuuint64_t)a.w_row_bytes, (cuuint64_t)wrows};
             const cuuint64_t strides[1] = {(cuuint64_t)a.w_row_bytes};
             const cuuint32_t box[2] = {(cuuint32_t)(U * 16), (cuuint32_t)BM};
             if (!encode(&tm_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.W, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
                 return cudaErrorInvalidValue;
         } else {                              // rows wider than a box dimension: 16-byte units
-            const cuuint64_t dims[3] = {16, (cuuint64_t)(a.w_row_bytes / 16), (cuuint64_t)a.N};
+            const cuuint64_t dims[3] = {16, (cuuint64_t)(a.w_row_bytes / 16), (cuuint64_t)wrows};
             const cuuint64_t strides[2] = {16, (cuuint64_t)a.w_row_bytes};
             const cuuint32_t box[3] = {16, (cuuint32_t)U, (cuuint32_t)BM};
             if (!encode(&tm_raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.W, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -100,10 +101,18 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    const long long ntn = (a.N + BM - 1) / BM;
+    if (a.work != nullptr) {                // MoE: one CTA per (work item, weight-row tile)
+        const tma::MoeTiles moe{a.work, a.nwork, a.gstart, a.rowlist};
+        const long long ctas = ntn * a.max_work;
+        kern<<<(unsigned)ctas, tma::Warps<WT>::kThreads, L::alloc, stream>>>(
+            tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)ctas, moe);
+        return cudaGetLastError();
+    }
     // Tail split: when the last wave of whole tiles would leave at least half the SMs idle, the last
     // token-tile rows are computed as two K halves each (twice the CTAs at half the time); their output
     // rows are zeroed first and both halves add into them.
-    const long long ntn = (a.N + BM - 1) / BM, ntm = (a.M + BN - 1) / BN, T = ntn * ntm;
+    const long long ntm = (a.M + BN - 1) / BN, T = ntn * ntm;
     const int sms = sm_count();
     const long long nst = a.K / BK;
     long long split_rows = 0;
@@ -121,7 +130,7 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     }
     const dim3 grid((unsigned)(nfull + 2 * split_rows * ntn));
     kern<<<grid, tma::Warps<WT>::kThreads, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K,
-                                                    (int)ntn, (int)nfull);
+                                                    (int)ntn, (int)nfull, tma::MoeTiles{});
     return cudaGetLastError();
 }
 
@@ -152,6 +161,59 @@ cudaError_t run_gemm_w8a8_tma(const void* W, const void* X, void* out, long long
     const long long tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
     kern<<<(unsigned)tiles, w8tma::NTHREADS, w8tma::Smem::alloc, stream>>>(
         tm_w, tm_x, ws, xs, static_cast<__nv_bfloat16*>(out), (int)M, (int)N, (int)K);
+    return cudaGetLastError();
+}
+
+// MoE gather: block (w, c) copies rows 32c .. 32c + 31 of work item w.  The item's first gathered row
+// is the 4-aligned sum of the preceding items' counts, so every item starts on a 16-byte boundary of
+// the block-major scales (the alignment a TMA box coordinate needs).
+constexpr int GATHER_ROWS = 32;
+__global__ void __launch_bounds__(256) moe_gather_kernel(const MoeGatherArgs g) {
+    const int w = blockIdx.x;
+    if (w >= *g.nwork) return;
+    const int row0 = blockIdx.y * GATHER_ROWS;
+    const int count = g.work[3 * w + 2];
+    if (row0 >= count) return;
+    __shared__ int s_start;
+    __shared__ int s_tok[GATHER_ROWS];
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+        int acc = 0;
+        for (int i = lane; i < w; i += 32) acc += (g.work[3 * i + 2] + 3) & ~3;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            s_start = acc;
+            if (blockIdx.y == 0) g.gstart[w] = acc;
+        }
+    } else if (threadIdx.x < 64) {
+        const int j = row0 + lane;
+        s_tok[lane] = j < count ? g.rowlist[g.work[3 * w + 1] + j] / g.slots : -1;
+    }
+    __syncthreads();
+    const int nrows = min(GATHER_ROWS, count - row0);
+    const long long dst0 = s_start + row0;
+    // fp16 codes: the whole block copies one row at a time in 16-byte vectors
+    const long long kv = g.K / 8;
+    for (int j = 0; j < nrows; j++) {
+        const uint4* src = static_cast<const uint4*>(g.xh) + (long long)s_tok[j] * kv;
+        uint4* dst = static_cast<uint4*>(g.xg) + (dst0 + j) * kv;
+        for (long long i = threadIdx.x; i < kv; i += blockDim.x) dst[i] = src[i];
+    }
+    // block scales: lanes over the rows (one 128-byte segment per block index), warps over the blocks
+    const long long kb = g.K / 32;
+    if (lane < nrows) {
+        const int tok = s_tok[lane];
+        for (long long b = threadIdx.x >> 5; b < kb; b += blockDim.x >> 5) {
+            g.dTg[b * g.Rg + dst0 + lane] = g.dT[b * g.Mp + tok];
+            g.sTg[b * g.Rg + dst0 + lane] = g.sT[b * g.Mp + tok];
+        }
+    }
+}
+
+cudaError_t run_moe_gather(const MoeGatherArgs& g, cudaStream_t s) {
+    const dim3 grid((unsigned)g.max_work, (unsigned)((BN + GATHER_ROWS - 1) / GATHER_ROWS));
+    moe_gather_kernel<<<grid, 256, 0, s>>>(g);
     return cudaGetLastError();
 }
 

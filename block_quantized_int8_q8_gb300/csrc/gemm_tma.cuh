@@ -260,26 +260,51 @@ __device__ __forceinline__ void rescale_half(uint64_t (&acc2)[8], const uint32_t
     }
 }
 
+// MoE (MUL_MAT_ID) mode of the kernel: work item w = (expert, first rowlist entry, row count <= 128)
+// as the routing pass lists them, and the item's first row in the gathered operand (a multiple of 4).
+struct MoeTiles {
+    const int* work;         // [3 * max_work]: expert, start, count; null in dense mode
+    const int* nwork;        // number of valid items
+    const int* gstart;       // [max_work]
+    const int* rowlist;      // (token, slot) row of each routed entry, grouped by expert
+};
+
 template <int WT>
 __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
-                        float* __restrict__ out, int M, int N, int K, int ntn, int nfull) {
+                        float* __restrict__ out, int M, int N, int K, int ntn, int nfull, const MoeTiles moe) {
     using L = Smem<WT>;
     using B = Bars<WT>;
     constexpr int U = Geom<WT>::U, SS = Geom<WT>::SS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Tile of this CTA (weight-row tiles fastest).  CTAs past the first nfull take the remaining tiles
-    // in pairs: each pair splits its tile's K range in two halves and both add into a zeroed output
-    // (two addends onto zero: the f32 result does not depend on their order).
+    // Tile of this CTA (weight-row tiles fastest).  Dense: CTAs past the first nfull take the remaining
+    // tiles in pairs: each pair splits its tile's K range in two halves and both add into a zeroed
+    // output (two addends onto zero: the f32 result does not depend on their order).  MoE: CTA
+    // (item w, weight-row tile) multiplies expert e's rows by the item's gathered token rows; CTAs of
+    // items past the routed count leave at once.
     int tile = blockIdx.x, part = -1;
-    if (tile >= nfull) {
-        tile = nfull + ((tile - nfull) >> 1);
-        part = (blockIdx.x - nfull) & 1;
+    int n0, m0, wrow, mvalid, rl0 = 0;
+    if (moe.work != nullptr) {
+        const int w = blockIdx.x / ntn;
+        if (w >= *moe.nwork) return;                           // uniform over the CTA, nothing set up yet
+        n0 = (blockIdx.x % ntn) * BM;
+        wrow = moe.work[3 * w] * N + n0;
+        rl0 = moe.work[3 * w + 1];
+        mvalid = moe.work[3 * w + 2];
+        m0 = moe.gstart[w];
+    } else {
+        if (tile >= nfull) {
+            tile = nfull + ((tile - nfull) >> 1);
+            part = (blockIdx.x - nfull) & 1;
+        }
+        n0 = (tile % ntn) * BM;
+        m0 = (tile / ntn) * BN;
+        wrow = n0;
+        mvalid = M - m0;
     }
-    const int n0 = (tile % ntn) * BM, m0 = (tile / ntn) * BN;
     const int nstages = part < 0 ? K / BK : K / BK / 2;       // stages of this CTA's K range
     const int s0 = part < 0 ? 0 : part * nstages;
 
@@ -337,10 +362,10 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
                     if (!mbar_wait_relaxed(B::rempty(c, rs), ((t >> 1) & 1) ^ 1, c.abort_flag)) break;
                     mbar_arrive_expect_tx(B::rfull(c, rs), BM * U * 16);
                     if constexpr (U * 16 <= 256)
-                        tma_load_2d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, (t + s0 / SS) * U * 16, n0,
+                        tma_load_2d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, (t + s0 / SS) * U * 16, wrow,
                                     B::rfull(c, rs));
                     else
-                        tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * U, n0,
+                        tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * U, wrow,
                                     B::rfull(c, rs));
                 }
                 const int slot = s & (STAGES - 1);
@@ -455,7 +480,14 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(B::sfree(c, ss));
         }
-        // ---- store: rows n0 + 32q + 16h + 8e + tq, tokens m0 + 32cq + 8j + 2tc + {0, 1}
+        // ---- store: rows n0 + 32q + 16h + 8e + tq, token columns 32cq + 8j + 2tc + {0, 1} below mvalid;
+        // output row of a column: m0 + column (dense) or its rowlist entry (MoE)
+        int orow[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int col = EPI_COLS * cq + 8 * (i >> 1) + 2 * tc + (i & 1);
+            orow[i] = col >= mvalid ? -1 : (moe.work != nullptr ? moe.rowlist[rl0 + col] : m0 + col);
+        }
 #pragma unroll
         for (int h = 0; h < 2; h++) {
 #pragma unroll
@@ -466,13 +498,13 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
                 for (int jj = 0; jj < 4; jj++) {
                     float a0, a1;
                     f2_unpack(acc[h][4 * e + jj], a0, a1);
-                    const int m = m0 + EPI_COLS * cq + 8 * jj + 2 * tc;
+                    const int r0 = orow[2 * jj], r1 = orow[2 * jj + 1];
                     if (part < 0) {
-                        if (m < M) out[(long long)m * N + n] = a0;
-                        if (m + 1 < M) out[(long long)(m + 1) * N + n] = a1;
+                        if (r0 >= 0) out[(long long)r0 * N + n] = a0;
+                        if (r1 >= 0) out[(long long)r1 * N + n] = a1;
                     } else {
-                        if (m < M) atomicAdd(out + (long long)m * N + n, a0);
-                        if (m + 1 < M) atomicAdd(out + (long long)(m + 1) * N + n, a1);
+                        if (r0 >= 0) atomicAdd(out + (long long)r0 * N + n, a0);
+                        if (r1 >= 0) atomicAdd(out + (long long)r1 * N + n, a1);
                     }
                 }
             }

@@ -29,12 +29,38 @@ struct TmaGemmArgs {
     const void* xh;             // q8_1 shadow: fp16 codes [M][K]
     const float* dT;            // q8_1 shadow: d, block-major [K/32][Mp]
     const float* sT;            // q8_1 shadow: s, block-major [K/32][Mp]
-    float* out;                 // f32 [M][N]
+    float* out;                 // f32 [M][N] (MoE: [M*slots][N])
     long long w_row_bytes;
-    long long M, N, K, Mp;
+    long long M, N, K, Mp;      // MoE: M = gathered rows, Mp their block-major pitch
+    // MoE mode (work != null): the weights hold E experts of N rows; xh/dT/sT are the gathered operand
+    long long E = 1;
+    const int* work = nullptr;
+    const int* nwork = nullptr;
+    const int* gstart = nullptr;
+    const int* rowlist = nullptr;
+    int max_work = 0;
 };
 bool tma_gemm_supported(int wt, long long K);
 cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s);
+// MoE operand gather (gemm_tma.cu): the fp16 codes and block scales of each work item's token rows,
+// copied to rows gstart[w] .. gstart[w] + count - 1 of xg [Rg][K] / dTg, sTg [K/32][Rg]; gstart[w] is
+// the 4-aligned prefix sum of the preceding items' counts.  Rg >= M*slots + 3*max_work, Rg % 4 == 0.
+struct MoeGatherArgs {
+    const int* work;
+    const int* nwork;
+    const int* rowlist;
+    int slots, max_work;
+    const void* xh;             // q8_1 shadow of the M tokens
+    const float* dT;
+    const float* sT;
+    long long Mp, K;
+    int* gstart;
+    void* xg;
+    float* dTg;
+    float* sTg;
+    long long Rg;
+};
+cudaError_t run_moe_gather(const MoeGatherArgs& g, cudaStream_t s);
 // Per-channel W8A8 on the TMA-fed kernel (gemm_w8a8_tma.cuh): W = int8 [N][K] + f32 ws[N],
 // X = int8 [M][K] + f32 xs[M], out bf16 [M][N]; K % 64 == 0.
 cudaError_t run_gemm_w8a8_tma(const void* W, const void* X, void* out, long long M, long long N, long long K,

@@ -143,12 +143,14 @@ mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out,
  * Xq         : q8_1 activations for M tokens.
  * expert_ids : int32 [M][n_slots], device; ids[t][j] in [0, n_experts), distinct per token.
  * out        : f32 [M][n_slots][N]; out[t][j][:] = W_{ids[t][j]} applied to token t.
- * workspace  : caller-owned device scratch of at least mmq_gemm_id_workspace_bytes(M, n_slots,
- *              n_experts) bytes; its contents on entry do not matter.
- * Routing (count, scan, scatter) and the grouped product run on the device with no host
+ * workspace  : caller-owned device scratch of at least mmq_gemm_id_workspace_bytes(M, K, n_slots,
+ *              n_experts) bytes, 16-byte aligned; its contents on entry do not matter.  It holds the
+ *              routing lists and, for the TMA-fed kernel, a gathered copy of the routed token rows
+ *              (fp16 codes and block scales, about 2*K + K/4 bytes per (token, slot) row).
+ * Routing (count, scan, scatter), the gather and the grouped product run on the device with no host
  * synchronisation.  Out-of-range ids set MMQ_DEVERR_EXPERT_ID and their rows are left unwritten.
  */
-size_t mmq_gemm_id_workspace_bytes(int64_t M, int n_slots, int n_experts);
+size_t mmq_gemm_id_workspace_bytes(int64_t M, int64_t K, int n_slots, int n_experts);
 mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void* Xq,
                        const int32_t* expert_ids, int n_slots, float* out,
                        int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
@@ -161,9 +163,11 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
  * only their input and output buffers), which cannot provide mmq_gemm_id's workspace.
  * Arguments and results are those of mmq_gemm_id without the workspace.  The routing lists live in a
  * file-scope device array of MMQ_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the
- * library until the process exits; the call itself allocates nothing.  Problems whose routing lists
- * need more than that (mmq_gemm_id_workspace_bytes(M, n_slots, n_experts) > MMQ_NOALLOC_SCRATCH_BYTES)
- * are rejected with MMQ_ERR_WORKSPACE.  The first call on each device looks up the array's device
+ * library until the process exits; the call itself allocates nothing.  It runs the general kernel on
+ * the token rows in place (no gathered copy).  Problems whose routing lists need more than the array
+ * (per-expert counts, offsets and cursors, 12 bytes per work item with ceil(M*n_slots/128) + n_experts
+ * items, 4 bytes per (token, slot) row, each list rounded up to 256 bytes) are rejected with
+ * MMQ_ERR_WORKSPACE.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  All calls share the array: calls whose kernels may overlap on the GPU (unordered streams)
  * race and must be serialised by the caller.

@@ -38,7 +38,7 @@ def test_sizes(lib):
     assert api.weight_bytes(api.W8A8, 5, 64) == 5 * 64 + 20
     assert api.weight_bytes(api.Q4_K, 5, 100) == 0
     assert api.w8a8_act_bytes(7, 64) == 7 * 64 + 28
-    assert api.gemm_id_workspace_bytes(512, 8, 64) > 512 * 8 * 4
+    assert api.gemm_id_workspace_bytes(512, 4096, 8, 64) > 512 * 8 * (4 + 2 * 4096)
 
 
 FAKE = 1 << 20          # 16-byte aligned, never dereferenced: every case fails validation first
@@ -64,7 +64,7 @@ def test_quantize_and_gemm_id_validation(lib):
     assert lib.mmq_q8_1_prepare(FAKE, 4, 96, None) == 2
     assert lib.mmq_q8_1_prepare(None, 4, 64, None) == 1
     ok = (api.IQ1_M, FAKE, 4, FAKE, FAKE, 2, FAKE, 16, 128, 256)
-    need = api.gemm_id_workspace_bytes(16, 2, 4)
+    need = api.gemm_id_workspace_bytes(16, 256, 2, 4)
     assert lib.mmq_gemm_id(*ok, FAKE, need - 1, None) == 6          # workspace too small
     assert lib.mmq_gemm_id(*ok, None, need, None) == 6
     assert lib.mmq_gemm_id(api.W8A8, *ok[1:], FAKE, need, None) == 4

@@ -190,6 +190,35 @@ def test_gemm_id_matches_oracle(wtype, M, E, slots, N, K):
             assert _rel_err(out[t, j], ref[t, j]) <= TOL, (t, j)
 
 
+@pytest.mark.parametrize("wtype", BLOCK_TYPES)
+def test_gemm_id_tma_path_matches_oracle(wtype):
+    # K % 1024 == 0: every block type takes the TMA-fed kernel on the gathered operand; N = 260 leaves a
+    # ragged weight-row tile, uneven expert counts leave work items of every size
+    M, E, slots, N, K = 200, 5, 3, 260, 1024
+    pb = synth.make_problem(wtype, M, N, K, seed=57 + wtype, experts=E, slots=slots)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm_id(wtype, _dev(pb.W.reshape(-1)), E, xq, _dev(pb.ids), M, N, K).cpu().numpy()
+    ref = oracle.gemm_id(wtype, pb.W, E, q, d, s, pb.ids, N)
+    assert api.read_device_errors() == 0
+    for t in range(M):
+        for j in range(slots):
+            assert _rel_err(out[t, j], ref[t, j]) <= TOL, (t, j)
+
+
+def test_gemm_id_tma_path_skewed_routing():
+    # expert 0 receives every token's slot 0 (300 rows: work items of 128, 128 and 44 rows), the other
+    # experts share slot 1
+    M, E, slots, N, K = 300, 8, 2, 130, 1024
+    pb = synth.make_problem(synth.IQ1_M, M, N, K, seed=63, experts=E, slots=slots)
+    pb.ids[:, 0] = 0
+    pb.ids[:, 1] = 1 + np.arange(M) % (E - 1)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm_id(synth.IQ1_M, _dev(pb.W.reshape(-1)), E, xq, _dev(pb.ids), M, N, K).cpu().numpy()
+    ref = oracle.gemm_id(synth.IQ1_M, pb.W, E, q, d, s, pb.ids, N)
+    assert api.read_device_errors() == 0
+    assert _rel_err(out, ref) <= TOL
+
+
 def test_gemm_id_skewed_routing():
     # every token routes slot 0 to expert 0: one expert receives M rows (several token tiles)
     M, E, slots, N, K = 300, 8, 2, 130, 256
