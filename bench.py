@@ -71,16 +71,26 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# Source files that define each GEMM kernel (device code and its launch); a change to any of them
+# voids the DRAM traffic recorded for that kernel.
+KERNEL_SOURCES = {
+    "mmq_gemm_tma_kernel": ["gemm_tma.cuh", "gemm_tma.cu", "gemm.cuh", "mmq_device.cuh", "internal.h"],
+    "mmq_w8a8_tma_kernel": ["gemm_w8a8_tma.cuh", "gemm_tma.cu", "gemm.cuh", "mmq_device.cuh", "internal.h"],
+    "mmq_gemm_kernel": ["gemm.cuh", "gemm_q8_0.cu", "gemm_q4_0.cu", "gemm_q4_k.cu", "gemm_iq1_m.cu",
+                        "mmq_device.cuh", "internal.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_int8_q8_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per GEMM launch from the committed ncu summary, if taken on the current kernels."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -88,7 +98,7 @@ def recorded_traffic(workload: str):
     with open(path) as f:
         rec = json.load(f)
     ent = rec.get(workload)
-    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel") != kernel or ent.get("kernel_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -446,7 +456,7 @@ def main():
     tma_path = (not is_moe) and wt != synth.W8A8 and (wt != synth.IQ1_M or K % 1024 == 0)
     kernel = "mmq_w8a8_tma_kernel" if wt == synth.W8A8 else ("mmq_gemm_tma_kernel" if tma_path else "mmq_gemm_kernel")
     roofline = {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(name),
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(name, kernel),
                 "peak_source": f"{peak_src} dense bf16 burst (fp16 operands, same nominal rate)",
                 "flops_per_launch": ops}
     int8_peak = ffma = None
