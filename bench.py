@@ -327,7 +327,11 @@ def main():
             out = torch.empty((M, pb.ids.shape[1], N), dtype=torch.float32, device=dev)
             ws = torch.empty(api.gemm_id_workspace_bytes(M, K, pb.ids.shape[1], pb.experts), dtype=torch.uint8,
                              device=dev)
-            launches_per_step = 6           # quantize, 4 routing kernels, grouped GEMM
+            # quantize, routing (one single-block launch up to 65536 rows and 1024 experts, else four),
+            # operand gather, grouped GEMM
+            small = M * pb.ids.shape[1] <= 65536 and pb.experts <= 1024
+            moe_tma = K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
+            launches_per_step = (4 if small else 7) if moe_tma else 6
         else:
             out = torch.empty((M, N), dtype=torch.float32, device=dev)
             launches_per_step = 2           # quantize, GEMM
@@ -451,9 +455,9 @@ def main():
     gemm_avg = statistics.mean(gemm_ms) / 1e3
     achieved = ops / gemm_avg / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    # the dense block-type GEMM runs the TMA-fed kernel (IQ1_M when K % 1024 == 0), W8A8 its own
-    # TMA-fed kernel; MoE and the remaining shapes run the general kernel
-    tma_path = (not is_moe) and wt != synth.W8A8 and (wt != synth.IQ1_M or K % 1024 == 0)
+    # the block types run the TMA-fed kernel (dense and MoE; IQ1_M when K % 1024 == 0), W8A8 its own
+    # TMA-fed kernel; the remaining shapes run the general kernel
+    tma_path = wt != synth.W8A8 and K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
     kernel = "mmq_w8a8_tma_kernel" if wt == synth.W8A8 else ("mmq_gemm_tma_kernel" if tma_path else "mmq_gemm_kernel")
     roofline = {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(name, kernel),

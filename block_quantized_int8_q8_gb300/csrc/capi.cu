@@ -253,9 +253,12 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
     ws.rowlist = reinterpret_cast<int*>(wb + L.rowlist);
     ws.max_work = L.max_work;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s);
+    const bool tma = tma_gemm_supported((int)wtype, K) && (long long)n_experts * N < (1ll << 31) && L.Rg < (1ll << 31);
+    cudaError_t e = (tma && route_fused_supported(M, n_slots, n_experts))
+                        ? run_route_fused(expert_ids, (int)M, n_slots, n_experts, BN, ws, s)
+                        : run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "mmq_gemm_id routing");
-    if (tma_gemm_supported((int)wtype, K) && (long long)n_experts * N < (1ll << 31) && L.Rg < (1ll << 31)) {
+    if (tma) {
         // TMA-fed kernel: gather each work item's token rows, then one CTA per (item, weight-row tile)
         const Q81Layout X = q81_layout(M, K);
         const uint8_t* xb = static_cast<const uint8_t*>(Xq);
@@ -275,7 +278,9 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
         g.dTg = reinterpret_cast<float*>(wb + L.dTg);
         g.sTg = reinterpret_cast<float*>(wb + L.sTg);
         g.Rg = L.Rg;
-        e = run_moe_gather(g, s);
+        g.out = out;
+        g.N = N;
+        e = run_moe_gather(g, (int)wtype, s);
         if (e != cudaSuccess) return cuda_fail(e, "mmq_gemm_id gather");
         TmaGemmArgs a;
         a.W = W;

@@ -57,6 +57,13 @@ int sm_count() {
     return counts[dev];
 }
 
+// Largest K split (4, 2 or 1) of a MoE tail tile whose parts hold whole raw super-stages.
+int moe_kparts(int wt, long long K) {
+    const long long nst = K / BK;
+    const int ss = wt == WT_IQ1_M ? tma::Geom<WT_IQ1_M>::SS : tma::Geom<WT_Q4_0>::SS;
+    return nst % (4 * ss) == 0 ? 4 : (nst % (2 * ss) == 0 ? 2 : 1);
+}
+
 template <int WT>
 cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     using L = tma::Smem<WT>;
@@ -102,9 +109,9 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
         configured = true;
     }
     const long long ntn = (a.N + BM - 1) / BM;
-    if (a.work != nullptr) {                // MoE: one CTA per (work item, weight-row tile)
-        const tma::MoeTiles moe{a.work, a.nwork, a.gstart, a.rowlist};
-        const long long ctas = ntn * a.max_work;
+    if (a.work != nullptr) {                // MoE: one CTA per (work item, weight-row tile) + tail parts
+        const tma::MoeTiles moe{a.work, a.nwork, a.gstart, a.rowlist, sm_count(), moe_kparts(WT, a.K)};
+        const long long ctas = ntn * a.max_work + moe.sms;
         kern<<<(unsigned)ctas, tma::Warps<WT>::kThreads, L::alloc, stream>>>(
             tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)ctas, moe);
         return cudaGetLastError();
@@ -193,25 +200,68 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const MoeGatherArgs g) 
     __syncthreads();
     const int nrows = min(GATHER_ROWS, count - row0);
     const long long dst0 = s_start + row0;
-    // fp16 codes: the whole block copies one row at a time in 16-byte vectors
+    // fp16 codes: thread t copies 16-byte column t (+256...) of eight rows at a time (eight loads in flight)
     const long long kv = g.K / 8;
-    for (int j = 0; j < nrows; j++) {
-        const uint4* src = static_cast<const uint4*>(g.xh) + (long long)s_tok[j] * kv;
-        uint4* dst = static_cast<uint4*>(g.xg) + (dst0 + j) * kv;
-        for (long long i = threadIdx.x; i < kv; i += blockDim.x) dst[i] = src[i];
+    const uint4* __restrict__ xh = static_cast<const uint4*>(g.xh);
+    uint4* __restrict__ xg = static_cast<uint4*>(g.xg);
+    for (long long cidx = threadIdx.x; cidx < kv; cidx += blockDim.x) {
+        for (int j0 = 0; j0 < nrows; j0 += 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+                if (j0 + u < nrows) v[u] = xh[(long long)s_tok[j0 + u] * kv + cidx];
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+                if (j0 + u < nrows) xg[(dst0 + j0 + u) * kv + cidx] = v[u];
+        }
     }
-    // block scales: lanes over the rows (one 128-byte segment per block index), warps over the blocks
+    // outputs of tail tiles computed in K parts (they add into zero): this item's rows, those tiles' columns
+    {
+        int nf, r;
+        const int ntn = (int)((g.N + BM - 1) / BM);
+        if (tma::tail_split(*g.nwork * ntn, g.sms, g.kparts, nf, r) > 0) {
+            for (int rt = 0; rt < ntn; rt++) {
+                if (w * ntn + rt < nf) continue;
+                const long long c0 = (long long)rt * BM, nc = min((long long)BM, g.N - c0);
+                for (int j = 0; j < nrows; j++) {
+                    float* o = g.out + (long long)g.rowlist[g.work[3 * w + 1] + row0 + j] * g.N + c0;
+                    for (long long i = threadIdx.x; i < nc; i += blockDim.x) o[i] = 0.f;
+                }
+            }
+        }
+    }
+    // block scales: lanes over the rows (one 128-byte segment per block index), warps over the blocks,
+    // four blocks in flight per lane
     const long long kb = g.K / 32;
     if (lane < nrows) {
         const int tok = s_tok[lane];
-        for (long long b = threadIdx.x >> 5; b < kb; b += blockDim.x >> 5) {
-            g.dTg[b * g.Rg + dst0 + lane] = g.dT[b * g.Mp + tok];
-            g.sTg[b * g.Rg + dst0 + lane] = g.sT[b * g.Mp + tok];
+        const long long nw = blockDim.x >> 5;
+        for (long long b0 = threadIdx.x >> 5; b0 < kb; b0 += 4 * nw) {
+            float dv[4], sv[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const long long b = b0 + u * nw;
+                if (b < kb) {
+                    dv[u] = g.dT[b * g.Mp + tok];
+                    sv[u] = g.sT[b * g.Mp + tok];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const long long b = b0 + u * nw;
+                if (b < kb) {
+                    g.dTg[b * g.Rg + dst0 + lane] = dv[u];
+                    g.sTg[b * g.Rg + dst0 + lane] = sv[u];
+                }
+            }
         }
     }
 }
 
-cudaError_t run_moe_gather(const MoeGatherArgs& g, cudaStream_t s) {
+cudaError_t run_moe_gather(const MoeGatherArgs& gin, int wt, cudaStream_t s) {
+    MoeGatherArgs g = gin;
+    g.sms = sm_count();
+    g.kparts = moe_kparts(wt, g.K);
     const dim3 grid((unsigned)g.max_work, (unsigned)((BN + GATHER_ROWS - 1) / GATHER_ROWS));
     moe_gather_kernel<<<grid, 256, 0, s>>>(g);
     return cudaGetLastError();

@@ -267,7 +267,25 @@ struct MoeTiles {
     const int* nwork;        // number of valid items
     const int* gstart;       // [max_work]
     const int* rowlist;      // (token, slot) row of each routed entry, grouped by expert
+    int sms;                 // multiprocessors (one CTA each)
+    int kparts;              // largest K split (1, 2 or 4) that keeps whole raw super-stages per part
 };
+
+// Tail split of T tiles over `sms` one-CTA-per-SM slots: when the last wave holds r tiles and P*r CTAs
+// still fit in one wave, those r tiles are computed as P parts of their K range each (P = 4 or 2, at
+// most kparts).  The first nf = T - r tiles run whole.  Returns log2(P) (0: no split).
+__host__ __device__ __forceinline__ int tail_split(int T, int sms, int kparts, int& nf, int& r) {
+    nf = T;
+    r = 0;
+    if (sms <= 0 || T <= sms) return 0;
+    const int rr = T - (T - 1) / sms * sms;
+    const int lg = (kparts >= 4 && 4 * rr <= sms) ? 2 : ((kparts >= 2 && 2 * rr <= sms) ? 1 : 0);
+    if (lg > 0) {
+        nf = T - rr;
+        r = rr;
+    }
+    return lg;
+}
 
 template <int WT>
 __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
@@ -285,12 +303,20 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     // output (two addends onto zero: the f32 result does not depend on their order).  MoE: CTA
     // (item w, weight-row tile) multiplies expert e's rows by the item's gathered token rows; CTAs of
     // items past the routed count leave at once.
-    int tile = blockIdx.x, part = -1;
+    int tile = blockIdx.x, part = -1, lgparts = 1;
     int n0, m0, wrow, mvalid, rl0 = 0;
     if (moe.work != nullptr) {
-        const int w = blockIdx.x / ntn;
-        if (w >= *moe.nwork) return;                           // uniform over the CTA, nothing set up yet
-        n0 = (blockIdx.x % ntn) * BM;
+        // the tile count is known on the device only: CTAs past the tiles (and their tail parts) leave
+        int nf, r;
+        lgparts = tail_split(*moe.nwork * ntn, moe.sms, moe.kparts, nf, r);
+        if (tile >= nf) {
+            const int ci = tile - nf;
+            if (ci >= (r << lgparts)) return;                  // uniform over the CTA, nothing set up yet
+            tile = nf + (ci >> lgparts);
+            part = ci & ((1 << lgparts) - 1);
+        }
+        const int w = tile / ntn;
+        n0 = (tile % ntn) * BM;
         wrow = moe.work[3 * w] * N + n0;
         rl0 = moe.work[3 * w + 1];
         mvalid = moe.work[3 * w + 2];
@@ -305,7 +331,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         wrow = n0;
         mvalid = M - m0;
     }
-    const int nstages = part < 0 ? K / BK : K / BK / 2;       // stages of this CTA's K range
+    const int nstages = part < 0 ? K / BK : (K / BK) >> lgparts;   // stages of this CTA's K range
     const int s0 = part < 0 ? 0 : part * nstages;
 
     Ctx c;
@@ -425,12 +451,27 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         const int cq = warp >> 2;
         const int tq = lane >> 2, tc = lane & 3;
         const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + EPI_COLS * cq;
+        // a warp whose token columns all lie past the tile's valid columns (a partly filled MoE tile, the
+        // last dense token tile) only takes part in the hand-offs
+        const bool active = EPI_COLS * cq < mvalid;
         uint64_t acc[2][8];                     // [half][4e + j]: packed f32 pair, tokens 8j + 2tc + {0, 1}
 #pragma unroll
         for (int h = 0; h < 2; h++)
 #pragma unroll
             for (int a = 0; a < 8; a++) acc[h][a] = 0ull;
-        for (int s = 0; s < nstages; s++) {
+        for (int s = 0; s < (active ? 0 : nstages); s++) {      // idle warp: hand-offs only
+            const int sb = s & (NSB - 1), ss = s % SC;
+            if (!mbar_wait(B::sfull(c, ss), (s / SC) & 1, c.abort_flag)) break;
+            if (!mbar_wait(B::accf(c, sb), (s / NSB) & 1, c.abort_flag)) break;
+            tc_fence_after();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(B::acce(c, sb));
+                mbar_arrive(B::sfree(c, ss));
+            }
+        }
+        for (int s = 0; s < (active ? nstages : 0); s++) {
             const int sb = s & (NSB - 1), ss = s % SC;
             if (!mbar_wait(B::sfull(c, ss), (s / SC) & 1, c.abort_flag)) break;
             if (!mbar_wait(B::accf(c, sb), (s / NSB) & 1, c.abort_flag)) break;

@@ -59,8 +59,11 @@ struct MoeGatherArgs {
     float* dTg;
     float* sTg;
     long long Rg;
+    float* out;                 // MoE output [M*slots][N]: rows of tiles split along K are zeroed here
+    long long N;
+    int sms = 0, kparts = 1;    // set by run_moe_gather
 };
-cudaError_t run_moe_gather(const MoeGatherArgs& g, cudaStream_t s);
+cudaError_t run_moe_gather(const MoeGatherArgs& g, int wt, cudaStream_t s);
 // Per-channel W8A8 on the TMA-fed kernel (gemm_w8a8_tma.cuh): W = int8 [N][K] + f32 ws[N],
 // X = int8 [M][K] + f32 xs[M], out bf16 [M][N]; K % 64 == 0.
 cudaError_t run_gemm_w8a8_tma(const void* W, const void* X, void* out, long long M, long long N, long long K,
@@ -90,6 +93,13 @@ struct RouteWorkspace {
 };
 cudaError_t run_route(const int32_t* ids, int M, int slots, int E, int tile_n, const RouteWorkspace& ws,
                       cudaStream_t s);
+// The same lists from one single-block launch (route.cu), for small problems; writes work, nwork and
+// rowlist only.
+constexpr int ROUTE_FUSED_MAX_EXPERTS = 1024;
+constexpr long long ROUTE_FUSED_MAX_ROWS = 1 << 16;
+bool route_fused_supported(long long M, int slots, int E);
+cudaError_t run_route_fused(const int32_t* ids, int M, int slots, int E, int tile_n, const RouteWorkspace& ws,
+                            cudaStream_t s);
 
 // Per-translation-unit device error words: read, OR into *bits, clear.
 cudaError_t read_clear_errors_quantize(unsigned* bits, cudaStream_t s);

@@ -205,6 +205,22 @@ def test_gemm_id_tma_path_matches_oracle(wtype):
             assert _rel_err(out[t, j], ref[t, j]) <= TOL, (t, j)
 
 
+@pytest.mark.parametrize("E", [38, 40])
+def test_gemm_id_tma_tail_split(E):
+    # more (work item, row tile) pairs than one wave of CTAs on a 152-SM part: 38 items x 5 row tiles
+    # leave 38 tiles in the last wave (split in 4 K parts), 40 x 5 leave 48 (split in 2); each part adds
+    # into an output zeroed by the gather pass
+    M, slots, N, K = 1000, 2, 640, 1024
+    pb = synth.make_problem(synth.Q4_0, M, N, K, seed=67 + E, experts=E, slots=slots)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm_id(synth.Q4_0, _dev(pb.W.reshape(-1)), E, xq, _dev(pb.ids), M, N, K).cpu().numpy()
+    ref = oracle.gemm_id(synth.Q4_0, pb.W, E, q, d, s, pb.ids, N)
+    assert api.read_device_errors() == 0
+    for t in range(0, M, 7):
+        for j in range(slots):
+            assert _rel_err(out[t, j], ref[t, j]) <= TOL, (t, j)
+
+
 def test_gemm_id_tma_path_skewed_routing():
     # expert 0 receives every token's slot 0 (300 rows: work items of 128, 128 and 44 rows), the other
     # experts share slot 1
