@@ -101,10 +101,13 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
         if (!encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.sT, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
-    auto kern = tma::mmq_gemm_tma_kernel<WT>;
+    auto kern = tma::mmq_gemm_tma_kernel<WT, false>;
+    auto kern_moe = tma::mmq_gemm_tma_kernel<WT, true>;
     static bool configured = false;       // per instantiation; the attribute is per function
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern_moe, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -112,7 +115,7 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     if (a.work != nullptr) {                // MoE: one CTA per (work item, weight-row tile) + tail parts
         const tma::MoeTiles moe{a.work, a.nwork, a.gstart, a.rowlist, sm_count(), moe_kparts(WT, a.K)};
         const long long ctas = ntn * a.max_work + moe.sms;
-        kern<<<(unsigned)ctas, tma::Warps<WT>::kThreads, L::alloc, stream>>>(
+        kern_moe<<<(unsigned)ctas, tma::Warps<WT>::kThreads, L::alloc, stream>>>(
             tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)ctas, moe);
         return cudaGetLastError();
     }

@@ -287,7 +287,7 @@ __host__ __device__ __forceinline__ int tail_split(int T, int sms, int kparts, i
     return lg;
 }
 
-template <int WT>
+template <int WT, bool MOE>
 __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     // items past the routed count leave at once.
     int tile = blockIdx.x, part = -1, lgparts = 1;
     int n0, m0, wrow, mvalid, rl0 = 0;
-    if (moe.work != nullptr) {
+    if constexpr (MOE) {
         // the tile count is known on the device only: CTAs past the tiles (and their tail parts) leave
         int nf, r;
         lgparts = tail_split(*moe.nwork * ntn, moe.sms, moe.kparts, nf, r);
@@ -527,7 +527,10 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             const int col = EPI_COLS * cq + 8 * (i >> 1) + 2 * tc + (i & 1);
-            orow[i] = col >= mvalid ? -1 : (moe.work != nullptr ? moe.rowlist[rl0 + col] : m0 + col);
+            if constexpr (MOE)
+                orow[i] = col >= mvalid ? -1 : moe.rowlist[rl0 + col];
+            else
+                orow[i] = col >= mvalid ? -1 : m0 + col;
         }
 #pragma unroll
         for (int h = 0; h < 2; h++) {
