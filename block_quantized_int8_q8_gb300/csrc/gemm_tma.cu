@@ -174,10 +174,10 @@ cudaError_t run_gemm_w8a8_tma(const void* W, const void* X, void* out, long long
     return cudaGetLastError();
 }
 
-// MoE gather: block (w, c) copies rows 32c .. 32c + 31 of work item w.  The item's first gathered row
-// is the 4-aligned sum of the preceding items' counts, so every item starts on a 16-byte boundary of
-// the block-major scales (the alignment a TMA box coordinate needs).
-constexpr int GATHER_ROWS = 32;
+// MoE gather: block (w, c) copies rows GATHER_ROWS*c .. GATHER_ROWS*(c+1) - 1 of work item w.  The
+// item's first gathered row is the 4-aligned sum of the preceding items' counts, so every item starts on
+// a 16-byte boundary of the block-major scales (the alignment a TMA box coordinate needs).
+constexpr int GATHER_ROWS = 8;          // eight rows per block: enough blocks in flight to fill every SM
 __global__ void __launch_bounds__(256) moe_gather_kernel(const MoeGatherArgs g) {
     const int w = blockIdx.x;
     if (w >= *g.nwork) return;
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const MoeGatherArgs g) 
             s_start = acc;
             if (blockIdx.y == 0) g.gstart[w] = acc;
         }
-    } else if (threadIdx.x < 64) {
+    } else if (threadIdx.x < 32 + GATHER_ROWS) {
         const int j = row0 + lane;
         s_tok[lane] = j < count ? g.rowlist[g.work[3 * w + 1] + j] / g.slots : -1;
     }
