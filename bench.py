@@ -287,8 +287,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="token count M in place of the workload's (same weights and K; a token-count study)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.tokens > 0:
+        # a derived workload: the named one with M tokens (same weights, K, seed and routing recipe)
+        derived = f"{args.workload}_m{args.tokens}"
+        synth.WORKLOADS[derived] = dict(synth.WORKLOADS[args.workload], M=args.tokens)
+        args.workload = derived
 
     if args.impl == "reference":
         return run_reference(args)

@@ -116,17 +116,24 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
         const tma::MoeTiles moe{a.work, a.nwork, a.gstart, a.rowlist, sm_count(), moe_kparts(WT, a.K)};
         const long long ctas = ntn * a.max_work + moe.sms;
         kern_moe<<<(unsigned)ctas, tma::Warps<WT>::kThreads, L::alloc, stream>>>(
-            tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)ctas, moe);
+            tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)ctas, 0, moe);
         return cudaGetLastError();
     }
-    // Tail split: when the last wave of whole tiles would leave at least half the SMs idle, the last
-    // token-tile rows are computed as two K halves each (twice the CTAs at half the time); their output
-    // rows are zeroed first and both halves add into them.
+    // Small grids: when all tiles fit in half the SMs or fewer, every tile runs as P = 2..16 parts of its K
+    // range (P tiles' worth of CTAs, each 1/P of the stages) adding into a zeroed output.
+    // Tail split: otherwise, when the last wave of whole tiles would leave at least half the SMs idle, the
+    // last token-tile rows run as two K halves each; their output rows are zeroed first.
     const long long ntm = (a.M + BN - 1) / BN, T = ntn * ntm;
     const int sms = sm_count();
     const long long nst = a.K / BK;
+    constexpr int SS = tma::Geom<WT>::SS;
     long long split_rows = 0;
-    if (sms > 0 && T > sms && nst % (2 * tma::Geom<WT>::SS) == 0) {
+    int lgp = 1;
+    if (sms > 0 && 2 * T <= sms && nst % (2 * SS) == 0) {
+        lgp = 1;
+        while (lgp < 4 && (T << (lgp + 1)) <= sms && nst % ((long long)SS << (lgp + 1)) == 0) lgp++;
+        split_rows = ntm;
+    } else if (sms > 0 && T > sms && nst % (2 * SS) == 0) {
         const long long r = T - (T - 1) / sms * sms;          // tiles in the last wave
         if (2 * r <= sms) split_rows = (r + ntn - 1) / ntn;
         if (split_rows >= ntm) split_rows = 0;
@@ -138,9 +145,9 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
                                               stream);
         if (e != cudaSuccess) return e;
     }
-    const dim3 grid((unsigned)(nfull + 2 * split_rows * ntn));
+    const dim3 grid((unsigned)(nfull + (split_rows * ntn << lgp)));
     kern<<<grid, tma::Warps<WT>::kThreads, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K,
-                                                    (int)ntn, (int)nfull, tma::MoeTiles{});
+                                                    (int)ntn, (int)nfull, lgp, tma::MoeTiles{});
     return cudaGetLastError();
 }
 

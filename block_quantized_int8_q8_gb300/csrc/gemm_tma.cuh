@@ -291,7 +291,8 @@ template <int WT, bool MOE>
 __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
-                        float* __restrict__ out, int M, int N, int K, int ntn, int nfull, const MoeTiles moe) {
+                        float* __restrict__ out, int M, int N, int K, int ntn, int nfull, int lgp,
+                        const MoeTiles moe) {
     using L = Smem<WT>;
     using B = Bars<WT>;
     constexpr int U = Geom<WT>::U, SS = Geom<WT>::SS;
@@ -299,10 +300,10 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Tile of this CTA (weight-row tiles fastest).  Dense: CTAs past the first nfull take the remaining
-    // tiles in pairs: each pair splits its tile's K range in two halves and both add into a zeroed
-    // output (two addends onto zero: the f32 result does not depend on their order).  MoE: CTA
-    // (item w, weight-row tile) multiplies expert e's rows by the item's gathered token rows; CTAs of
-    // items past the routed count leave at once.
+    // tiles in groups of 2^lgp, each CTA one part of its tile's K range, all adding into a zeroed output
+    // (with two parts the f32 result does not depend on their order).  MoE: CTA (item, weight-row tile)
+    // multiplies expert e's rows by the item's gathered token rows; CTAs of items past the routed count
+    // leave at once.
     int tile = blockIdx.x, part = -1, lgparts = 1;
     int n0, m0, wrow, mvalid, rl0 = 0;
     if constexpr (MOE) {
@@ -323,8 +324,10 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         m0 = moe.gstart[w];
     } else {
         if (tile >= nfull) {
-            tile = nfull + ((tile - nfull) >> 1);
-            part = (blockIdx.x - nfull) & 1;
+            const int ci = tile - nfull;
+            tile = nfull + (ci >> lgp);
+            part = ci & ((1 << lgp) - 1);
+            lgparts = lgp;
         }
         n0 = (tile % ntn) * BM;
         m0 = (tile / ntn) * BN;
