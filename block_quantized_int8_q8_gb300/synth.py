@@ -14,6 +14,8 @@ by uniform codes and uniform scales:
   value is the scale);
 * Q8_0 codes uniform in [-127, 127]; Q4_0 / Q4_K codes uniform in 0..15; Q4_K 6-bit sc, m uniform 0..63;
 * IQ1_M: g uniform in {-1, 0, 1} per value, sign uniform per 8 values, 3-bit s uniform 0..7 per 16;
+* Q6_K: 6-bit codes uniform 0..63, int8 sub-block scales uniform in [-128, 127] per 16 values, f16 d per
+  256 values;
 * W8A8: int8 weights and activations uniform in [-127, 127], f32 per-row scales ~ U(1e-3, 1e-2);
 * MoE routing: each token picks `n_slots` distinct experts uniformly.
 
@@ -25,6 +27,9 @@ Byte layouts (per weight row, blocks back to back; rows back to back):
   IQ1_M 76 B / 256: 64 B 2-bit codes (value i at bits 2(i%4) of byte i/4, code = g+1) | 4 B sign bits
                     (bit j: values 8j..8j+7, 1 = minus) | 6 B little-endian bit stream of 16 three-bit s
                     | f16 d
+  Q6_K 224 B / 256: int8 sc[16] | f16 d | 14 B zero | four 48 B stage records j: 32 B, byte i = low
+                    nibble of code 64j+i | low nibble of code 64j+32+i << 4; 16 B, byte i = high 2 bits of
+                    codes 64j+i, 64j+16+i, 64j+32+i, 64j+48+i at bits 0-1, 2-3, 4-5, 6-7
   W8A8            : int8 W [N][K] then f32 ws [N]   (activations: int8 X [M][K] then f32 xs [M])
 """
 from __future__ import annotations
@@ -33,13 +38,13 @@ from dataclasses import dataclass
 
 import numpy as np
 
-Q8_0, Q4_0, Q4_K, IQ1_M, W8A8 = 0, 1, 2, 3, 4
-TYPE_NAMES = {Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k", IQ1_M: "iq1_m", W8A8: "w8a8"}
+Q8_0, Q4_0, Q4_K, IQ1_M, W8A8, Q6_K = 0, 1, 2, 3, 4, 5
+TYPE_NAMES = {Q8_0: "q8_0", Q4_0: "q4_0", Q4_K: "q4_k", IQ1_M: "iq1_m", W8A8: "w8a8", Q6_K: "q6_k"}
 TYPE_IDS = {v: k for k, v in TYPE_NAMES.items()}
 
 #: bytes per block and values per block, per weight type
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 144, IQ1_M: 76}
-BLOCK_VALUES = {Q8_0: 32, Q4_0: 32, Q4_K: 256, IQ1_M: 256}
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 144, IQ1_M: 76, Q6_K: 224}
+BLOCK_VALUES = {Q8_0: 32, Q4_0: 32, Q4_K: 256, IQ1_M: 256, Q6_K: 256}
 
 
 def weight_row_bytes(wtype: int, K: int) -> int:
@@ -103,6 +108,13 @@ class IQ1_MFields:
 
 
 @dataclass
+class Q6_KFields:
+    d: np.ndarray      # f16 [N, K/256]
+    sc: np.ndarray     # int8 [N, K/16]
+    code: np.ndarray   # uint8 [N, K] in 0..63
+
+
+@dataclass
 class W8A8Fields:
     W: np.ndarray      # int8 [N, K]
     ws: np.ndarray     # f32 [N]
@@ -123,6 +135,10 @@ def draw_fields(g: np.random.Generator, wtype: int, N: int, K: int):
         return IQ1_MFields(d=f16_scales(g, (N, K // 256)), s=g.integers(0, 8, size=(N, K // 16), dtype=np.uint8),
                            neg=g.integers(0, 2, size=(N, K // 8), dtype=np.uint8),
                            g=(g.integers(0, 3, size=(N, K), dtype=np.int8) - 1).astype(np.int8))
+    if wtype == Q6_K:
+        return Q6_KFields(d=f16_scales(g, (N, K // 256)),
+                          sc=g.integers(-128, 128, size=(N, K // 16), dtype=np.int16).astype(np.int8),
+                          code=g.integers(0, 64, size=(N, K), dtype=np.uint8))
     if wtype == W8A8:
         return W8A8Fields(W=g.integers(-127, 128, size=(N, K), dtype=np.int16).astype(np.int8),
                           ws=g.uniform(1e-3, 1e-2, size=N).astype(np.float32))
@@ -166,6 +182,19 @@ def pack(wtype: int, f) -> np.ndarray:
         blk[..., 68:74] = _bits_le(f.s.reshape(N, nsb, 16), 3)
         blk[..., 74:76] = _f16_bytes(f.d)
         return blk.reshape(N, -1)
+    if wtype == Q6_K:
+        N, K = f.code.shape
+        nsb = K // 256
+        blk = np.zeros((N, nsb, 224), np.uint8)
+        blk[..., 0:16] = f.sc.reshape(N, nsb, 16).view(np.uint8)
+        blk[..., 16:18] = _f16_bytes(f.d)
+        c = f.code.reshape(N, nsb, 4, 64)
+        lo, hi = c & 15, c >> 4
+        rec = np.empty((N, nsb, 4, 48), np.uint8)
+        rec[..., 0:32] = lo[..., :32] | (lo[..., 32:] << 4)
+        rec[..., 32:48] = hi[..., 0:16] | (hi[..., 16:32] << 2) | (hi[..., 32:48] << 4) | (hi[..., 48:64] << 6)
+        blk[..., 32:224] = rec.reshape(N, nsb, 192)
+        return blk.reshape(N, -1)
     if wtype == W8A8:
         return np.concatenate([f.W.reshape(-1).view(np.uint8), f.ws.view(np.uint8)])
     raise ValueError(f"unknown weight type {wtype}")
@@ -201,6 +230,7 @@ WORKLOADS = {
     "w8a8_m4096":     dict(wtype=W8A8, M=4096, N=1536, K=4096, seed=1014),
     "iq1_m_moe":      dict(wtype=IQ1_M, M=512, N=1536, K=4096, seed=1005, experts=64, slots=8),
     "iq1_m_dense":    dict(wtype=IQ1_M, M=512, N=4096, K=4096, seed=1006),
+    "q6_k_ffn_down":  dict(wtype=Q6_K, M=2048, N=4096, K=11008, seed=1007),
 }
 
 

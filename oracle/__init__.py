@@ -8,7 +8,8 @@ link or call anything here, and nothing here is shared with them: the oracle is 
 Functions and the passages they follow (page title, section):
   quantize_q8_1   "08 · R1 — int8 MMQ prefill GEMM", §2.2 q8_1 activation pipeline and §3.2 reference
   decode          "08 · R1", §2.1/§2.2 (Q8_0, Q4_0, Q4_K unsigned nibbles + min term);
-                  "CUDA: add IQ1_M to MMQ", Design (IQ1_M fold 8g±1, per-16 scale d(2s+1)/8)
+                  "CUDA: add IQ1_M to MMQ", Design (IQ1_M fold 8g±1, per-16 scale d(2s+1)/8);
+                  "08 · R1", §2.2 (q6_K: 6-bit grid minus 32, int8 scales per 16 elements)
   partials        "08 · R1", §2.1 (exact in-block int32 dot)
   gemm/gemm_rows  "When the Product Won't Collapse: A Negative Result on int8 Tensor-Core MMQ", §2
                   (blockwise contraction) with the §3.2 per-block correction of "08 · R1"
@@ -33,7 +34,7 @@ _lib = None
 # The pin suite's mutation self-test points this at a deliberately broken build of the oracle.
 _LIB_OVERRIDE = os.environ.get("MMQ_ORACLE_LIB")
 
-Q8_0, Q4_0, Q4_K, IQ1_M, W8A8 = 0, 1, 2, 3, 4
+Q8_0, Q4_0, Q4_K, IQ1_M, W8A8, Q6_K = 0, 1, 2, 3, 4, 5
 
 
 def build(force: bool = False, out: str | None = None, defines=()) -> str:
@@ -99,7 +100,7 @@ def quantize_q8_1(x: np.ndarray):
 
 
 def group_size(wtype: int) -> int:
-    return 16 if wtype == IQ1_M else 32
+    return 16 if wtype in (IQ1_M, Q6_K) else 32
 
 
 def decode(wtype: int, W: np.ndarray, N: int, K: int):
@@ -113,7 +114,7 @@ def decode(wtype: int, W: np.ndarray, N: int, K: int):
 
 
 def partials(wtype: int, xq: np.ndarray, wq: np.ndarray) -> np.ndarray:
-    """Exact per-group int32 dots I[m, n, g] (groups of 32, or 16 for IQ1_M)."""
+    """Exact per-group int32 dots I[m, n, g] (groups of 32, or 16 for IQ1_M and Q6_K)."""
     xq = np.ascontiguousarray(xq, dtype=np.int8)
     wq = np.ascontiguousarray(wq, dtype=np.int8)
     M, K = xq.shape

@@ -14,6 +14,9 @@
  *   [IQ]  "CUDA: add IQ1_M to MMQ" (llama.cpp pull request #304), PR description and "Design".
  *   [W8]  "INT8 W8A8 GEMM — Prefill (M > 32) — gfx928 / SGLang TP4 + TP8", §1 "M = 3072 prefill"
  *         and §2 (int32 accumulation, scale epilogue, bf16 output, mismatch 0 / max_abs_error 0.0).
+ *   [R1] §2.2 also fixes q6_K's arithmetic: a 6-bit grid 0..63 moved to the signed domain by
+ *         subtracting 32, scales on 16-element sub-blocks, so each 32-k chunk carries two integer dots
+ *         multiplied by (d*sc0, d*sc1) ("The K-quant signed domain"; "The q6_K per-16 loop").
  *
  * Mutation switches (MUT_*): each plants one plausible mistake.  They are never defined in a normal
  * build; the pin suite's self-test compiles each mutant and checks that some pin fails on it.
@@ -34,6 +37,10 @@
  *                      1 -> -1/8) | 6 B = 16 three-bit sub-scales s, little-endian bit stream (s_h for
  *                      elements 16h..16h+15) | f16 d
  *   W8A8             : int8 W [N][K] with f32 ws [N]; int8 X [M][K] with f32 xs [M]
+ *   Q6_K (224 B/256) : int8 sc[16] (sc_h for elements 16h..16h+15) | f16 d | 14 B zero | four 48 B
+ *                      stage records j = 0..3: 32 B low nibbles, byte i = element 64j+i (low) |
+ *                      element 64j+32+i (high), then 16 B high pairs, byte i = bits 4-5 of elements
+ *                      64j+i (bits 0-1), 64j+16+i (bits 2-3), 64j+32+i (bits 4-5), 64j+48+i (bits 6-7)
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -43,7 +50,10 @@
 #include <omp.h>
 #endif
 
-enum { OR_Q8_0 = 0, OR_Q4_0 = 1, OR_Q4_K = 2, OR_IQ1_M = 3, OR_W8A8 = 4 };
+enum { OR_Q8_0 = 0, OR_Q4_0 = 1, OR_Q4_K = 2, OR_IQ1_M = 3, OR_W8A8 = 4, OR_Q6_K = 5 };
+
+/* Block types of the blockwise product (W8A8 has its own entry point). */
+static int block_type(int wtype) { return (wtype >= 0 && wtype <= 3) || wtype == OR_Q6_K; }
 
 /* ---------------------------------------------------------------- scalar helpers */
 
@@ -140,9 +150,10 @@ int oracle_quantize_q8_1(const float* x, int64_t M, int64_t K, int8_t* q, float*
  *   Q4_0 : wq = nib - 8,         wsc = d          (w = d (q - 8))
  *   Q4_K : wq = nib (unsigned),  wsc = d*sc_b, wmin = dmin*m_b   [R1] §2.2 rank-1 min term
  *   IQ1_M: wq = 8g + (+1|-1),    wsc = d*(2s+1)/8 per 16 values  [IQ] Design (exact fold)
+ *   Q6_K : wq = q - 32,          wsc = d*sc_h per 16 values      [R1] §2.2 (signed domain, sub-scales)
  *   W8A8 : wq = W, one scale per row (handled by oracle_w8a8).
  */
-static int group_size(int wtype) { return wtype == OR_IQ1_M ? 16 : 32; }
+static int group_size(int wtype) { return (wtype == OR_IQ1_M || wtype == OR_Q6_K) ? 16 : 32; }
 
 static void decode_row(int wtype, const uint8_t* row, int64_t K, int8_t* wq, float* wsc, float* wmin) {
     if (wtype == OR_Q8_0) {
@@ -220,6 +231,25 @@ static void decode_row(int wtype, const uint8_t* row, int64_t K, int8_t* wq, flo
                 wsc[sb * 16 + h] = (dd * (float)(2u * sv + 1u)) * 0.125f;
             }
         }
+    } else if (wtype == OR_Q6_K) {
+        for (int64_t sb = 0; sb < K / 256; sb++) {
+            const uint8_t* blk = row + sb * 224;
+            float dd = half_to_float(rd16(blk + 16));
+            for (int h = 0; h < 16; h++) wsc[sb * 16 + h] = dd * (float)(int8_t)blk[h];
+            for (int j = 0; j < 4; j++) {
+                const uint8_t* lo = blk + 32 + 48 * j;
+                const uint8_t* hi = lo + 32;
+                for (int e = 0; e < 64; e++) {
+                    int low = e < 32 ? (lo[e] & 15) : (lo[e - 32] >> 4);
+#ifdef MUT_Q6K_HIGH_PAIR
+                    int high = (hi[e % 16] >> (2 * (e % 4))) & 3;
+#else
+                    int high = (hi[e % 16] >> (2 * (e / 16))) & 3;
+#endif
+                    wq[sb * 256 + 64 * j + e] = (int8_t)((low | (high << 4)) - 32);
+                }
+            }
+        }
     }
 }
 
@@ -229,20 +259,21 @@ static int64_t row_bytes(int wtype, int64_t K) {
         case OR_Q4_0: return K / 32 * 18;
         case OR_Q4_K: return K / 256 * 144;
         case OR_IQ1_M: return K / 256 * 76;
+        case OR_Q6_K: return K / 256 * 224;
         default: return K;
     }
 }
 
 static int check_k(int wtype, int64_t K) {
     if (K <= 0) return 1;
-    if ((wtype == OR_Q4_K || wtype == OR_IQ1_M) && K % 256 != 0) return 1;
+    if ((wtype == OR_Q4_K || wtype == OR_IQ1_M || wtype == OR_Q6_K) && K % 256 != 0) return 1;
     if (K % 32 != 0) return 1;
     return 0;
 }
 
 /* Decode a whole [N][K] weight matrix: wq [N][K], wsc [N][K/G], wmin [N][K/32] (Q4_K only). */
 int oracle_decode(int wtype, const uint8_t* W, int64_t N, int64_t K, int8_t* wq, float* wsc, float* wmin) {
-    if (wtype < 0 || wtype > 3 || check_k(wtype, K)) return 1;
+    if (!block_type(wtype) || check_k(wtype, K)) return 1;
     const int64_t G = group_size(wtype);
     for (int64_t n = 0; n < N; n++)
         decode_row(wtype, W + n * row_bytes(wtype, K), K, wq + n * K, wsc + n * (K / G),
@@ -257,7 +288,7 @@ int oracle_decode(int wtype, const uint8_t* W, int64_t N, int64_t K, int8_t* wq,
  */
 int oracle_partials(int wtype, const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
                     int32_t* P) {
-    if (wtype < 0 || wtype > 4 || check_k(wtype, K)) return 1;
+    if (wtype < 0 || wtype > 5 || check_k(wtype, K)) return 1;
     const int64_t G = group_size(wtype), ng = K / G;
 #pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < M; m++)
@@ -283,13 +314,13 @@ int oracle_partials(int wtype, const int8_t* xq, const int8_t* wq, int64_t M, in
  * Per block b, in this order (f32, round to nearest, no fused multiply-add):
  *   Q8_0/Q4_0 : acc = acc + ((xd * wsc) * (float)I)
  *   Q4_K      : acc = acc + (((xd * wsc) * (float)I) - (wmin * s))
- *   IQ1_M     : for h = 0, 1: acc = acc + ((xd * wsc_h) * (float)I_h)      (per-16 halves)
+ *   IQ1_M,Q6_K: for h = 0, 1: acc = acc + ((xd * wsc_h) * (float)I_h)      (per-16 halves)
  */
 static float block_dot_row(int wtype, const int8_t* xq, const float* xd, const float* xs,
                            const int8_t* wq, const float* wsc, const float* wmin, int64_t K) {
     float acc = 0.0f;
     for (int64_t b = 0; b < K / 32; b++) {
-        if (wtype == OR_IQ1_M) {
+        if (wtype == OR_IQ1_M || wtype == OR_Q6_K) {
             for (int h = 0; h < 2; h++) {
                 int32_t I = 0;
                 for (int64_t k = b * 32 + 16 * h; k < b * 32 + 16 * h + 16; k++)
@@ -325,7 +356,7 @@ static float block_dot_row(int wtype, const int8_t* xq, const float* xd, const f
  */
 int oracle_gemm(int wtype, const uint8_t* W, const int8_t* xq, const float* xd, const float* xs,
                 int64_t M, int64_t N, int64_t K, float* out) {
-    if (wtype < 0 || wtype > 3 || check_k(wtype, K)) return 1;
+    if (!block_type(wtype) || check_k(wtype, K)) return 1;
     const int64_t G = group_size(wtype);
     int8_t* wq = (int8_t*)malloc((size_t)(N * K));
     float* wsc = (float*)malloc((size_t)(N * (K / G)) * sizeof(float));
@@ -346,7 +377,7 @@ int oracle_gemm(int wtype, const uint8_t* W, const int8_t* xq, const float* xd, 
 /* Same product for a chosen subset of activation rows (rows[i] in [0, M)): out [nrows][N]. */
 int oracle_gemm_rows(int wtype, const uint8_t* W, const int8_t* xq, const float* xd, const float* xs,
                      int64_t M, int64_t N, int64_t K, const int64_t* rows, int64_t nrows, float* out) {
-    if (wtype < 0 || wtype > 3 || check_k(wtype, K)) return 1;
+    if (!block_type(wtype) || check_k(wtype, K)) return 1;
     for (int64_t i = 0; i < nrows; i++)
         if (rows[i] < 0 || rows[i] >= M) return 1;
     const int64_t G = group_size(wtype);
@@ -409,7 +440,7 @@ int oracle_w8a8_partials(const int8_t* W, const int8_t* X, int64_t M, int64_t N,
 int oracle_gemm_id(int wtype, const uint8_t* W, int64_t n_experts, const int8_t* xq, const float* xd,
                    const float* xs, const int32_t* ids, int64_t n_slots, int64_t M, int64_t N, int64_t K,
                    float* out) {
-    if (wtype < 0 || wtype > 3 || check_k(wtype, K) || n_experts <= 0 || n_slots <= 0) return 1;
+    if (!block_type(wtype) || check_k(wtype, K) || n_experts <= 0 || n_slots <= 0) return 1;
     for (int64_t i = 0; i < M * n_slots; i++)
         if (ids[i] < 0 || ids[i] >= n_experts) return 1;
     const int64_t G = group_size(wtype), nb = K / 32, rb = row_bytes(wtype, K);

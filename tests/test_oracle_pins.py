@@ -125,7 +125,7 @@ def test_quantizer_invariants(dist):
 
 
 # ---------------------------------------------------------------------------------- decoders
-@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M])
+@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M, synth.Q6_K])
 def test_decoder_round_trip_with_generator_packer(wtype):
     N, K = 7, 1024
     f = synth.draw_fields(np.random.default_rng(3 + wtype), wtype, N, K)
@@ -143,6 +143,11 @@ def test_decoder_round_trip_with_generator_packer(wtype):
         dm = np.repeat(f.dmin.astype(np.float64), 8, axis=1)
         assert np.array_equal(wsc.astype(np.float64), d * f.sc)      # exact: 11-bit x 6-bit
         assert np.array_equal(wmin.astype(np.float64), dm * f.m)
+    elif wtype == synth.Q6_K:
+        # "08 · R1" §2.2: the 6-bit grid moves to the signed domain by subtracting 32
+        assert np.array_equal(wq.astype(np.int32), f.code.astype(np.int32) - 32)
+        d = np.repeat(f.d.astype(np.float64), 16, axis=1)
+        assert np.array_equal(wsc.astype(np.float64), d * f.sc)      # exact: 11-bit x 8-bit
     else:
         neg = np.repeat(f.neg, 8, axis=1).astype(np.int32)
         assert np.array_equal(wq.astype(np.int32), 8 * f.g.astype(np.int32) + np.where(neg == 1, -1, 1))
@@ -168,6 +173,33 @@ def test_q4_k_hand_built_single_field_blocks():
     assert list(wmin[0]) == [0, 0, 0, 0, 0, 126, 0, 0]
     nz = np.flatnonzero(wq[0])
     assert list(nz) == [70, 100] and wq[0, 70] == 9 and wq[0, 100] == 4
+
+
+def test_q6_k_hand_built_single_field_blocks():
+    # d = 0.25; sc[2] = -3, sc[13] = 127; every code 32 (value 0) except: value 33 (stage 0, low nibble in
+    # byte 1 high half, high pair in byte 1 bits 4-5) = 63 -> +31; value 64+18 (stage 1, low nibble in
+    # byte 18 low half, high pair in byte 2 bits 2-3) = 0 -> -32; value 192+50 (stage 3, byte 18 high
+    # half, high pair in byte 2 bits 6-7) = 47 -> +15.
+    blk = np.zeros(224, np.uint8)
+    blk[2] = np.uint8(np.int8(-3).view(np.uint8))
+    blk[13] = 127
+    blk[16:18] = np.array([0.25], np.float16).view(np.uint8)
+    for j in range(4):                 # all codes 32: low nibble 0, high pair 2 -> 0b10 in every field
+        blk[32 + 48 * j: 64 + 48 * j] = 0x00
+        blk[64 + 48 * j: 80 + 48 * j] = 0xAA
+    r0, r1, r3 = 32, 32 + 48, 32 + 3 * 48
+    blk[r0 + 1] = 0xF0                                  # value 33 low nibble 15
+    blk[r0 + 32 + 1] = (0xAA & ~(3 << 4)) | (3 << 4)    # value 33 high pair 3 -> code 63
+    blk[r1 + 18] = 0x00                                 # value 82 low nibble 0
+    blk[r1 + 32 + 2] = 0xAA & ~(3 << 2)                 # value 64+18 high pair 0 -> code 0
+    blk[r3 + 18] = 0xF0                                 # value 192+50 low nibble 15
+    blk[r3 + 32 + 2] = 0xAA & ~(3 << 6)                 # high pair of value 192+50 = 0... code 15
+    blk[r3 + 32 + 2] |= (2 << 6)                        # ... pair 2: code 32 + 15 = 47
+    wq, wsc, _ = oracle.decode(synth.Q6_K, blk[None], 1, 256)
+    assert wsc[0, 2] == -0.75 and wsc[0, 13] == 31.75 and wsc[0, 0] == 0.0
+    nz = np.flatnonzero(wq[0])
+    assert list(nz) == [33, 82, 242], list(nz)
+    assert (wq[0, 33], wq[0, 82], wq[0, 242]) == (31, -32, 15)
 
 
 def test_q4_0_hand_built_nibble_order():
@@ -205,7 +237,7 @@ def test_iq1_m_fold_exhaustive_and_value_set():
 
 
 # ---------------------------------------------------------------------------------- integer partials
-@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M, synth.W8A8])
+@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M, synth.W8A8, synth.Q6_K])
 def test_partials_brute_force(wtype):
     g = np.random.default_rng(20 + wtype)
     M, N, K = 5, 6, 512
@@ -213,7 +245,7 @@ def test_partials_brute_force(wtype):
     wq = g.integers(-127 if wtype != synth.IQ1_M else -9, 128 if wtype != synth.IQ1_M else 10,
                     size=(N, K)).astype(np.int8)
     P = oracle.partials(wtype, xq, wq)
-    G = 16 if wtype == synth.IQ1_M else 32
+    G = 16 if wtype in (synth.IQ1_M, synth.Q6_K) else 32
     for m in range(M):
         for n in range(N):
             for gi in range(K // G):
@@ -248,6 +280,9 @@ def _dequant_f64(wtype, f):
         s = np.repeat(f.s.astype(np.float64), 16, 1)
         delta = np.where(np.repeat(f.neg, 8, 1) == 1, -0.125, 0.125)
         return d * (2 * s + 1) * (f.g + delta)
+    if wtype == synth.Q6_K:
+        d = np.repeat(f.d.astype(np.float64), 256, 1)
+        return d * np.repeat(f.sc.astype(np.float64), 16, 1) * (f.code.astype(np.float64) - 32)
     raise ValueError
 
 
@@ -257,7 +292,7 @@ def _term_magnitudes(wtype, f, q, d):
     W = _dequant_f64(wtype, f)
     xh = np.repeat(d.astype(np.float64), 32, 1) * q
     M, K = q.shape
-    G = 16 if wtype == synth.IQ1_M else 32
+    G = 16 if wtype in (synth.IQ1_M, synth.Q6_K) else 32
     mags = np.zeros((M, W.shape[0]))
     if wtype == synth.Q4_K:
         pos = np.repeat(f.d.astype(np.float64), 256, 1) * np.repeat(f.sc, 32, 1) * f.code
@@ -271,7 +306,7 @@ def _term_magnitudes(wtype, f, q, d):
     return W, xh, mags
 
 
-@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M])
+@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M, synth.Q6_K])
 @pytest.mark.parametrize("shape", [(3, 5, 256), (17, 9, 1024)])
 def test_blockwise_matches_f64_dequant_matmul(wtype, shape):
     M, N, K = shape
@@ -283,7 +318,7 @@ def test_blockwise_matches_f64_dequant_matmul(wtype, shape):
     out = oracle.gemm(wtype, W, q, d, s, N)
     Wd, xh, mags = _term_magnitudes(wtype, f, q, d)
     ref = xh @ Wd.T
-    G = 16 if wtype == synth.IQ1_M else 32
+    G = 16 if wtype in (synth.IQ1_M, synth.Q6_K) else 32
     # per group: scale product, product with I, (Q4_K: min product, stored s, difference), then the
     # running sum -- at most K/G + 4 roundings of 2^-24 against the sum of product magnitudes
     bound = (K // G + 4) * 2.0 ** -24 * mags
@@ -293,7 +328,7 @@ def test_blockwise_matches_f64_dequant_matmul(wtype, shape):
     assert bound.max() < 1e-4 * np.abs(ref).max()
 
 
-@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.IQ1_M])
+@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.IQ1_M, synth.Q6_K])
 def test_blockwise_with_unit_scales_is_integer_matmul(wtype):
     # d = 1 for weights and activations: every block term is its integer dot, so the product is the
     # plain integer matmul of the codes (exact in f32 here: |out| < 2^24).
@@ -303,6 +338,8 @@ def test_blockwise_with_unit_scales_is_integer_matmul(wtype):
     f.d[...] = np.float16(1.0)
     if wtype == synth.IQ1_M:
         f.s[...] = 0          # (2s+1)/8 = 1/8 per 16: scale 1/8, integer values 8g+-1 -> out = dot/8
+    if wtype == synth.Q6_K:
+        f.sc[...] = 1         # d * sc = 1 per 16: integer values code - 32
     W = synth.pack(wtype, f)
     q = g.integers(-127, 128, size=(M, K)).astype(np.int8)
     d = np.ones((M, K // 32), np.float32)
@@ -312,6 +349,8 @@ def test_blockwise_with_unit_scales_is_integer_matmul(wtype):
         wint = f.q.astype(np.int64)
     elif wtype == synth.Q4_0:
         wint = f.code.astype(np.int64) - 8
+    elif wtype == synth.Q6_K:
+        wint = f.code.astype(np.int64) - 32
     else:
         wint = 8 * f.g.astype(np.int64) + np.where(np.repeat(f.neg, 8, 1) == 1, -1, 1)
     ref = q.astype(np.int64) @ wint.T
