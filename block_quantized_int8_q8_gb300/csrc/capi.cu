@@ -34,12 +34,15 @@ long long weight_row_bytes(mmq_type t, long long K) {
         case MMQ_Q4_K: return K / 256 * 144;
         case MMQ_IQ1_M: return K / 256 * 76;
         case MMQ_W8A8: return K;
+        case MMQ_Q6_K: return K / 256 * 224;
     }
     return -1;
 }
 
-bool known_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_W8A8; }
-bool block_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_IQ1_M; }
+bool known_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_Q6_K; }
+bool block_type(int t) { return (t >= MMQ_Q8_0 && t <= MMQ_IQ1_M) || t == MMQ_Q6_K; }
+// Types the general kernel takes (debug partials, mmq_gemm_id_noalloc, shapes the TMA kernel does not).
+bool general_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_W8A8; }
 
 // Shape rules shared by every GEMM entry point.
 mmq_status check_shape(mmq_type t, long long M, long long N, long long K) {
@@ -142,7 +145,7 @@ size_t mmq_q8_1_bytes(int64_t M, int64_t K) {
 
 size_t mmq_weight_bytes(mmq_type t, int64_t N, int64_t K) {
     if (!known_type(t) || N < 0 || K <= 0) return 0;
-    if (block_type(t) && (t == MMQ_Q4_K || t == MMQ_IQ1_M) && K % 256 != 0) return 0;
+    if (block_type(t) && (t == MMQ_Q4_K || t == MMQ_IQ1_M || t == MMQ_Q6_K) && K % 256 != 0) return 0;
     if (K % 32 != 0) return 0;
     if (t == MMQ_W8A8) return (size_t)(N * K + 4 * N);
     return (size_t)(N * weight_row_bytes(t, K));
@@ -202,6 +205,7 @@ mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out, in
         const cudaError_t e = run_gemm_w8a8_tma(W, Xq, out, M, N, K, reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm");
     }
+    if (!general_type(wtype)) return MMQ_ERR_UNSUPPORTED;
     GemmParams p = dense_params(wtype, W, Xq, out, M, N, K);
     const cudaError_t e =
         dispatch(wtype, p, MODE_PROD, false, (int)((M + BN - 1) / BN), reinterpret_cast<cudaStream_t>(stream));
@@ -211,6 +215,7 @@ mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out, in
 mmq_status mmq_gemm_debug_partials(mmq_type wtype, const void* W, const void* Xq, int32_t* partials, int64_t M,
                                    int64_t N, int64_t K, mmq_stream_t stream) {
     if (!known_type(wtype)) return MMQ_ERR_INVALID_ARG;
+    if (!general_type(wtype)) return MMQ_ERR_UNSUPPORTED;
     mmq_status st = check_shape(wtype, M, N, K);
     if (st != MMQ_OK) return st;
     if (M == 0 || N == 0) return MMQ_OK;
@@ -254,6 +259,7 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
     ws.max_work = L.max_work;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool tma = tma_gemm_supported((int)wtype, K) && (long long)n_experts * N < (1ll << 31) && L.Rg < (1ll << 31);
+    if (!tma && !general_type(wtype)) return MMQ_ERR_UNSUPPORTED;
     cudaError_t e = (tma && route_fused_supported(M, n_slots, n_experts))
                         ? run_route_fused(expert_ids, (int)M, n_slots, n_experts, BN, ws, s)
                         : run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s);

@@ -59,7 +59,7 @@ __device__ __forceinline__ uint4 split2_record(float v) {
     return make_uint4(h, h, h, 0u);
 }
 
-enum WType { WT_Q8_0 = 0, WT_Q4_0 = 1, WT_Q4_K = 2, WT_IQ1_M = 3, WT_W8A8 = 4 };
+enum WType { WT_Q8_0 = 0, WT_Q4_0 = 1, WT_Q4_K = 2, WT_IQ1_M = 3, WT_W8A8 = 4, WT_Q6_K = 5 };
 enum Mode { MODE_PROD = 0, MODE_DEBUG = 1 };
 
 constexpr int BM = 128;             // weight rows per tile (MMA M, TMEM lanes)

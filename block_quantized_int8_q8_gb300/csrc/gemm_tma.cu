@@ -3,8 +3,9 @@
 // Four tensor maps per call, encoded on the host with the driver's cuTensorMapEncodeTiled (looked up
 // once through the runtime's driver entry-point query, so the library needs no -lcuda):
 //   raw  : the weight bytes [N][row_bytes] uint8; box 128 rows x U*16 bytes (one raw super-stage) as a
-//          2-D box when it fits a box dimension (Q4_0, Q4_K), else as [N][row_bytes/16][16] with a
-//          3-D box of U 16-byte units (Q8_0, IQ1_M); rows past N read as zeros.
+//          2-D box when it fits a box dimension (Q4_0, Q4_K, Q6_K), else as [N][row_bytes/16][16] with a
+//          3-D box of U 16-byte units (Q8_0, IQ1_M); rows past N read as zeros.  Q6_K's 224-byte
+//          super-block is read as a 240-byte box (an odd number of 16-byte units in shared memory).
 //   b    : the q8_1 shadow's fp16 codes [M][K]; box 128 tokens x 64 k, 128-byte swizzle (the MMA's
 //          K-major operand layout); tokens past M read as zeros.
 //   xd/xs: the block-major scales d^T, s^T [K/32][Mp]; box 2 blocks x 128 tokens.
@@ -279,7 +280,7 @@ cudaError_t run_moe_gather(const MoeGatherArgs& gin, int wt, cudaStream_t s) {
 
 bool tma_gemm_supported(int wt, long long K) {
     if (wt == WT_IQ1_M) return K % 1024 == 0;
-    return (wt == WT_Q8_0 || wt == WT_Q4_0 || wt == WT_Q4_K) && K % 256 == 0;
+    return (wt == WT_Q8_0 || wt == WT_Q4_0 || wt == WT_Q4_K || wt == WT_Q6_K) && K % 256 == 0;
 }
 
 cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s) {
@@ -288,6 +289,7 @@ cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s) {
         case WT_Q4_0: return launch<WT_Q4_0>(a, s);
         case WT_Q4_K: return launch<WT_Q4_K>(a, s);
         case WT_IQ1_M: return launch<WT_IQ1_M>(a, s);
+        case WT_Q6_K: return launch<WT_Q6_K>(a, s);
     }
     return cudaErrorInvalidValue;
 }

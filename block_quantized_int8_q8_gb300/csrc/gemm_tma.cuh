@@ -30,7 +30,13 @@
 namespace mmq {
 namespace tma {
 
-constexpr int STAGES = 4;            // operand ring (A converted by the converters, B by TMA)
+// Operand ring (A converted by the converters, B by TMA): four stages; q6_K carries two A tiles per stage
+// (its sub-block scale split over two exactly representable operands) and three stages to fit.
+template <int WT> struct Ring {
+    static constexpr int kStages = (WT == WT_Q6_K) ? 3 : 4;
+    static constexpr int kATiles = (WT == WT_Q6_K) ? 2 : 1;
+    static constexpr int kAStage = kATiles * A_STAGE_BYTES;
+};
 constexpr int SC = 8;                // scale ring depth (converters run up to 4 stages ahead of the
                                      // MMA, the epilogue trails it by up to 2)
 constexpr int RAW_SLOTS = 2;
@@ -44,7 +50,7 @@ constexpr int EPI_CHUNKS = EPI_COLS / 16;      // 16-column TMEM loads per block
 // leave 96 registers per thread (20 warps); IQ1_M's unpack is the heaviest per row and gets four (22
 // warps, 80 registers).
 template <int WT> struct Warps {
-    static constexpr int kConv = (WT == WT_IQ1_M) ? 4 : 2;
+    static constexpr int kConv = (WT == WT_IQ1_M || WT == WT_Q6_K) ? 4 : 2;
     static constexpr int kRowsPerConv = BM / (kConv * 32);
     static constexpr int kConv0 = EPI_WARPS;
     static constexpr int kMma = kConv0 + kConv;
@@ -53,19 +59,24 @@ template <int WT> struct Warps {
 };
 constexpr long long ABORT_DRAIN_CYCLES = 2000000;   // ~1 ms: lets in-flight TMA writes land after an abort
 
-// Raw super-stage geometry: U 16-byte units per weight row, SS 64-k operand stages per super-stage.
+// Raw super-stage geometry: U 16-byte units per weight row in shared memory (the TMA box width; odd, so
+// the converters' 16-byte row reads are conflict-free), UG units per super-stage in global memory, SS 64-k
+// operand stages per super-stage.
 template <int WT> struct Geom;
-template <> struct Geom<WT_Q8_0> { static constexpr int U = 17, SS = 4; };    // 8 blocks x 34 B
-template <> struct Geom<WT_Q4_0> { static constexpr int U = 9, SS = 4; };     // 8 blocks x 18 B
-template <> struct Geom<WT_Q4_K> { static constexpr int U = 9, SS = 4; };     // one 144 B super-block
-template <> struct Geom<WT_IQ1_M> { static constexpr int U = 19, SS = 16; };  // four 76 B super-blocks
+template <> struct Geom<WT_Q8_0> { static constexpr int U = 17, UG = 17, SS = 4; };    // 8 blocks x 34 B
+template <> struct Geom<WT_Q4_0> { static constexpr int U = 9, UG = 9, SS = 4; };      // 8 blocks x 18 B
+template <> struct Geom<WT_Q4_K> { static constexpr int U = 9, UG = 9, SS = 4; };      // one 144 B super-block
+template <> struct Geom<WT_IQ1_M> { static constexpr int U = 19, UG = 19, SS = 16; };  // four 76 B super-blocks
+// q6_K: one 224 B super-block, read as a 240 B box (the 16 B past it belong to the next super-block or
+// are zero-filled past the row end, and are never read)
+template <> struct Geom<WT_Q6_K> { static constexpr int U = 15, UG = 14, SS = 4; };
 
 template <int WT> struct Smem {
     static constexpr bool kMin = WT == WT_Q4_K;               // Q4_K min term needs xs and wmn
     static constexpr int a_off = 0;
-    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr int b_off = a_off + Ring<WT>::kStages * Ring<WT>::kAStage;
     static constexpr int raw_slot = (BM * Geom<WT>::U * 16 + 1023) / 1024 * 1024;
-    static constexpr int raw_off = b_off + STAGES * B_STAGE_BYTES;
+    static constexpr int raw_off = b_off + Ring<WT>::kStages * B_STAGE_BYTES;
     // one scale slot: xd[2][128] (TMA) | xs[2][128] (TMA, Q4_K) | wd[2][128] | wmn[2][128] (Q4_K)
     static constexpr int xd_off = 0;
     static constexpr int xs_off = 1024;
@@ -74,7 +85,7 @@ template <int WT> struct Smem {
     static constexpr int sc_slot = kMin ? 4096 : 2048;
     static constexpr int sc_off = raw_off + RAW_SLOTS * raw_slot;
     static constexpr int bar_off = sc_off + SC * sc_slot;
-    static constexpr int n_bars = 2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NSB + 1;
+    static constexpr int n_bars = 2 * Ring<WT>::kStages + 2 * RAW_SLOTS + 2 * SC + 2 * NSB + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int total = misc_off + 16;
     static constexpr int alloc = total + 1024;                  // slack for 1024-byte alignment
@@ -130,10 +141,48 @@ __device__ __forceinline__ void load_raw(uint32_t rrow, RawA& r) {
     } else if constexpr (WT == WT_Q4_K) {
         raw_words<0, 4, 0>(rrow, r);                           // d, dmin, 12 B of scales
         raw_words<16 + 32 * J, 8, 4>(rrow, r);                 // codes of sub-blocks 2J, 2J+1
-    } else {
+    } else if constexpr (WT == WT_IQ1_M) {
         constexpr int sbk = J / 4, jj = J % 4;
         raw_words<76 * sbk + 16 * jj, 4, 0>(rrow, r);          // 64 two-bit codes
         raw_words<76 * sbk + 64, 3, 4>(rrow, r);               // signs, sub-scales, d
+    } else {
+        raw_words<0, 5, 0>(rrow, r);                           // sc[16], d
+        raw_words<32 + 48 * J, 12, 5>(rrow, r);                // stage record: 32 B low nibbles, 16 B high pairs
+    }
+}
+
+// q6_K, operand stage J of a super-block ("08 · R1 — int8 MMQ prefill GEMM", §2.2: 6-bit grid 0..63
+// moved to the signed domain by subtracting 32; scales on 16-element sub-blocks).  The int8 sub-block
+// scale sc = 16*sh + sl (sl in 0..15, sh in -8..7) is folded into two operands that fp16 holds exactly:
+// A1 = (q-32)*sl, |A1| <= 480, and A2 = (q-32)*16*sh, a multiple of 16 with |A2| <= 4096.  Two MMAs
+// add A1.B and A2.B into the block's accumulator, so it holds sum (q-32)*sc*x exactly (|.| <= 32*32*128*127
+// < 2^24) and the block scale is the super-block d.  Sub-block g (values 16g..16g+15 of the stage) is
+// operand chunks 2g, 2g+1 of both tiles.
+template <int J>
+__device__ __forceinline__ void q6k_stage_operands(const RawA& r, uint32_t at1, uint32_t at2, int row) {
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+        const int sc = (int)(int8_t)((r.w[J] >> (8 * g)) & 0xFFu);     // sub-block 4J+g
+        const uint32_t m1 = f2_to_h2((float)(sc & 15), (float)(sc & 15));
+        const uint32_t m2 = f2_to_h2((float)(16 * (sc >> 4)), (float)(16 * (sc >> 4)));
+        uint32_t h[8];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {                                   // values 16g+4k .. 16g+4k+3
+            const uint32_t lw = g < 2 ? r.w[5 + 4 * g + k] : (r.w[5 + 4 * (g - 2) + k] >> 4);
+            const uint32_t code = (lw & 0x0F0F0F0Fu) | (((r.w[13 + k] >> (2 * g)) & 0x03030303u) << 4);
+            u8x4_to_f16x4(code, 0x64206420u, h[2 * k], h[2 * k + 1]);  // 1024 + code - 1056 = code - 32
+        }
+        uint32_t a1[8], a2[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(a1[i]) : "r"(h[i]), "r"(m1));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(a2[i]) : "r"(h[i]), "r"(m2));
+        }
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            st_shared_v4(at1 + sw128_off(row, 2 * g + q), a1[4 * q], a1[4 * q + 1], a1[4 * q + 2], a1[4 * q + 3]);
+            st_shared_v4(at2 + sw128_off(row, 2 * g + q), a2[4 * q], a2[4 * q + 1], a2[4 * q + 2], a2[4 * q + 3]);
+        }
     }
 }
 
@@ -149,21 +198,21 @@ struct Ctx {
 
 template <int WT> struct Bars {
     __device__ static uint32_t full(const Ctx& c, int i) { return c.bar0 + 8u * i; }
-    __device__ static uint32_t empty(const Ctx& c, int i) { return c.bar0 + 8u * (STAGES + i); }
-    __device__ static uint32_t rfull(const Ctx& c, int i) { return c.bar0 + 8u * (2 * STAGES + i); }
-    __device__ static uint32_t rempty(const Ctx& c, int i) { return c.bar0 + 8u * (2 * STAGES + RAW_SLOTS + i); }
-    __device__ static uint32_t sfull(const Ctx& c, int i) { return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + i); }
+    __device__ static uint32_t empty(const Ctx& c, int i) { return c.bar0 + 8u * (Ring<WT>::kStages + i); }
+    __device__ static uint32_t rfull(const Ctx& c, int i) { return c.bar0 + 8u * (2 * Ring<WT>::kStages + i); }
+    __device__ static uint32_t rempty(const Ctx& c, int i) { return c.bar0 + 8u * (2 * Ring<WT>::kStages + RAW_SLOTS + i); }
+    __device__ static uint32_t sfull(const Ctx& c, int i) { return c.bar0 + 8u * (2 * Ring<WT>::kStages + 2 * RAW_SLOTS + i); }
     __device__ static uint32_t sfree(const Ctx& c, int i) {
-        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + SC + i);
+        return c.bar0 + 8u * (2 * Ring<WT>::kStages + 2 * RAW_SLOTS + SC + i);
     }
     __device__ static uint32_t accf(const Ctx& c, int i) {
-        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + i);
+        return c.bar0 + 8u * (2 * Ring<WT>::kStages + 2 * RAW_SLOTS + 2 * SC + i);
     }
     __device__ static uint32_t acce(const Ctx& c, int i) {
-        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + NSB + i);
+        return c.bar0 + 8u * (2 * Ring<WT>::kStages + 2 * RAW_SLOTS + 2 * SC + NSB + i);
     }
     __device__ static uint32_t done(const Ctx& c) {
-        return c.bar0 + 8u * (2 * STAGES + 2 * RAW_SLOTS + 2 * SC + 2 * NSB);
+        return c.bar0 + 8u * (2 * Ring<WT>::kStages + 2 * RAW_SLOTS + 2 * SC + 2 * NSB);
     }
 };
 
@@ -174,28 +223,34 @@ __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t raw) {
     using B = Bars<WT>;
     if (!c.ok) return;
     const int s = t * Geom<WT>::SS + J;
-    const int slot = s & (STAGES - 1), ss = s % SC;
-    if (!mbar_wait_relaxed(B::empty(c, slot), ((s / STAGES) & 1) ^ 1, c.abort_flag) ||
+    const int slot = s % Ring<WT>::kStages, ss = s % SC;
+    if (!mbar_wait_relaxed(B::empty(c, slot), ((s / Ring<WT>::kStages) & 1) ^ 1, c.abort_flag) ||
         !mbar_wait_relaxed(B::sfree(c, ss), ((s / SC) & 1) ^ 1, c.abort_flag)) {
         c.ok = false;
         return;
     }
-    const uint32_t at = c.sb + L::a_off + slot * A_STAGE_BYTES;
+    const uint32_t at = c.sb + L::a_off + slot * Ring<WT>::kAStage;
     const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
 #pragma unroll 1
     for (int rr = 0; rr < Warps<WT>::kRowsPerConv; rr++) {
         const int row = c.pt + rr * Warps<WT>::kConv * 32;
         RawA r;
         load_raw<WT, J>(raw + row * Geom<WT>::U * 16, r);
-        uint32_t h[32];
-        float wsc[2], wmn[2];
-        // the unpackers use only s % 4 (the stage's place in a 256-value super-block); K ranges start on
-        // super-stage boundaries, so the local index gives the same value and keeps it a compile-time one
-        unpack_a<WT, true>(r, s, h, wsc, wmn);
-        if (row >= c.rows_valid) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
+        float wsc[2], wmn[2] = {0.f, 0.f};
+        if constexpr (WT == WT_Q6_K) {
+            q6k_stage_operands<J>(r, at, at + A_STAGE_BYTES, row);
+            wsc[0] = wsc[1] = half_bits_to_float((uint16_t)(r.w[4] & 0xFFFFu));   // super-block d
+        } else {
+            uint32_t h[32];
+            // the unpackers use only s % 4 (the stage's place in a 256-value super-block); K ranges start
+            // on super-stage boundaries, so the local index gives the same value and keeps it a
+            // compile-time one
+            unpack_a<WT, true>(r, s, h, wsc, wmn);
 #pragma unroll
-        for (int q = 0; q < 8; q++)
-            st_shared_v4(at + sw128_off(row, q), h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+            for (int q = 0; q < 8; q++)
+                st_shared_v4(at + sw128_off(row, q), h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        }
+        if (row >= c.rows_valid) wsc[0] = wsc[1] = wmn[0] = wmn[1] = 0.f;
         st_shared_f32(scs + L::wd_off + 4 * row, wsc[0]);
         st_shared_f32(scs + L::wd_off + 4 * (BM + row), wsc[1]);
         if constexpr (L::kMin) {
@@ -295,7 +350,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
                         const MoeTiles moe) {
     using L = Smem<WT>;
     using B = Bars<WT>;
-    constexpr int U = Geom<WT>::U, SS = Geom<WT>::SS;
+    constexpr int U = Geom<WT>::U, UG = Geom<WT>::UG, SS = Geom<WT>::SS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -348,7 +403,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
 
     if (warp == Warps<WT>::kMma) {
         if (lane == 0) {
-            for (int i = 0; i < STAGES; i++) {
+            for (int i = 0; i < Ring<WT>::kStages; i++) {
                 mbar_init(B::full(c, i), Warps<WT>::kConv + 1);     // converter warps + the B load
                 mbar_init(B::empty(c, i), 1);
             }
@@ -391,14 +446,14 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
                     if (!mbar_wait_relaxed(B::rempty(c, rs), ((t >> 1) & 1) ^ 1, c.abort_flag)) break;
                     mbar_arrive_expect_tx(B::rfull(c, rs), BM * U * 16);
                     if constexpr (U * 16 <= 256)
-                        tma_load_2d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, (t + s0 / SS) * U * 16, wrow,
+                        tma_load_2d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, (t + s0 / SS) * UG * 16, wrow,
                                     B::rfull(c, rs));
                     else
-                        tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * U, wrow,
+                        tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * UG, wrow,
                                     B::rfull(c, rs));
                 }
-                const int slot = s & (STAGES - 1);
-                if (!mbar_wait_relaxed(B::empty(c, slot), ((s / STAGES) & 1) ^ 1, c.abort_flag)) break;
+                const int slot = s % Ring<WT>::kStages;
+                if (!mbar_wait_relaxed(B::empty(c, slot), ((s / Ring<WT>::kStages) & 1) ^ 1, c.abort_flag)) break;
                 mbar_arrive_expect_tx(B::full(c, slot), B_STAGE_BYTES);
                 tma_load_2d(c.sb + L::b_off + slot * B_STAGE_BYTES, &tm_b, BK * (s + s0), m0, B::full(c, slot));
                 const int ss = s % SC;
@@ -421,18 +476,22 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         const uint32_t b_smem = c.sb + L::b_off;
         for (int s = 0; s < nstages; s++) {
             if (*c.abort_flag) break;
-            const int slot = s & (STAGES - 1);
+            const int slot = s % Ring<WT>::kStages;
             const int sb = s & (NSB - 1);      // stage buffer: accumulators 2*sb (block 2s), 2*sb+1 (block 2s+1)
-            if (!mbar_wait(B::full(c, slot), (s / STAGES) & 1, c.abort_flag)) break;
+            if (!mbar_wait(B::full(c, slot), (s / Ring<WT>::kStages) & 1, c.abort_flag)) break;
             mbar_wait(B::acce(c, sb), ((s / NSB) & 1) ^ 1, c.abort_flag);
             tc_fence_after();
-            const uint64_t ad0 = sdesc_sw128(a_smem + slot * A_STAGE_BYTES);
+            const uint64_t ad0 = sdesc_sw128(a_smem + slot * Ring<WT>::kAStage);
             const uint64_t bd0 = sdesc_sw128(b_smem + slot * B_STAGE_BYTES);
 #pragma unroll
             for (int j = 0; j < 4; j++) {
                 const int buf = 2 * sb + (j >> 1);
                 // +32 bytes per 16-element K slice: +2 in the descriptor's address field
                 if (elect_one()) umma_f16(tmem_base + buf * BN, ad0 + 2 * j, bd0 + 2 * j, idesc, j & 1);
+                if constexpr (Ring<WT>::kATiles == 2) {       // q6_K: second operand tile, same block
+                    const uint64_t ad1 = sdesc_sw128(a_smem + slot * Ring<WT>::kAStage + A_STAGE_BYTES);
+                    if (elect_one()) umma_f16(tmem_base + buf * BN, ad1 + 2 * j, bd0 + 2 * j, idesc, 1u);
+                }
             }
             if (elect_one()) {
                 umma_commit(B::accf(c, sb));

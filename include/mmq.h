@@ -45,12 +45,20 @@
  *                            8j..8j+7; 0 -> delta=+1/8, 1 -> delta=-1/8) | 6 B little-endian bit stream
  *                            of 16 three-bit sub-scales s (s_h covers values 16h..16h+15) | f16 d;
  *                            value = d*(2s+1)*(g+delta)
+ *   Q6_K 224 B / 256 values: int8 sc[16] (sc_h covers values 16h..16h+15) | f16 d | 14 B zero | four
+ *                            48 B stage records j = 0..3: 32 B, byte i = low nibble of code 64j+i |
+ *                            low nibble of code 64j+32+i << 4; 16 B, byte i = high 2 bits of codes
+ *                            64j+i, 64j+16+i, 64j+32+i, 64j+48+i at bits 0-1, 2-3, 4-5, 6-7;
+ *                            code in 0..63, value = d*sc_h*(code-32)  ("08 · R1", §2.2: 6-bit grid,
+ *                            signed domain by subtracting 32, scales on 16-element sub-blocks)
  *   W8A8 weights           : int8 W[N][K] followed by f32 ws[N]        (mmq_weight_bytes)
  *   W8A8 activations       : int8 X[M][K] followed by f32 xs[M]        (mmq_w8a8_act_bytes)
  *   Weights are row-major over N: row n is its K/values-per-block blocks back to back.
  *
  * Shape rules: M >= 1, N >= 1 (any value; tails are masked).  K >= 256 and K % 256 == 0 for the block
- * types (Q8_0, Q4_0, Q4_K, IQ1_M); K % 64 == 0 for W8A8.  M*K and N*K below 2^31.
+ * types (Q8_0, Q4_0, Q4_K, IQ1_M, Q6_K); K % 64 == 0 for W8A8.  M*K and N*K below 2^31.
+ * Q6_K runs on the TMA-fed kernel only: mmq_gemm and mmq_gemm_id take it; mmq_gemm_debug_partials
+ * returns MMQ_ERR_UNSUPPORTED and mmq_gemm_id_noalloc MMQ_ERR_INVALID_ARG for it.
  */
 #ifndef MMQ_GB300_H
 #define MMQ_GB300_H
@@ -70,7 +78,8 @@ typedef enum {
     MMQ_Q4_0 = 1,
     MMQ_Q4_K = 2,
     MMQ_IQ1_M = 3,
-    MMQ_W8A8 = 4
+    MMQ_W8A8 = 4,
+    MMQ_Q6_K = 5
 } mmq_type;
 
 typedef enum {

@@ -35,6 +35,8 @@ def test_sizes(lib):
     assert api.weight_bytes(api.Q4_0, 5, 256) == 5 * 8 * 18
     assert api.weight_bytes(api.Q4_K, 5, 512) == 5 * 2 * 144
     assert api.weight_bytes(api.IQ1_M, 5, 512) == 5 * 2 * 76
+    assert api.weight_bytes(api.Q6_K, 5, 512) == 5 * 2 * 224
+    assert api.weight_bytes(api.Q6_K, 5, 100) == 0
     assert api.weight_bytes(api.W8A8, 5, 64) == 5 * 64 + 20
     assert api.weight_bytes(api.Q4_K, 5, 100) == 0
     assert api.w8a8_act_bytes(7, 64) == 7 * 64 + 28
@@ -70,6 +72,8 @@ def test_quantize_and_gemm_id_validation(lib):
     assert lib.mmq_gemm_id(api.W8A8, *ok[1:], FAKE, need, None) == 4
     assert lib.mmq_gemm_id(api.IQ1_M, FAKE, 0, *ok[3:], FAKE, need, None) == 1
     assert lib.mmq_gemm_debug_partials(api.Q4_K, FAKE, FAKE, FAKE, 4, 4, 128, None) == 2
+    assert lib.mmq_gemm_debug_partials(api.Q6_K, FAKE, FAKE, FAKE, 4, 4, 256, None) == 4   # TMA kernel only
+    assert lib.mmq_gemm(6, FAKE, FAKE, FAKE, 4, 4, 256, None) == 1                         # unknown type
     for s in range(7):
         assert lib.mmq_status_string(s)
     assert lib.mmq_read_device_errors(None, None) == 1

@@ -45,7 +45,7 @@ def _rel_err(got, ref):
     return float(np.abs(got.astype(np.float64) - ref).max() / (scale if scale > 0 else 1.0))
 
 
-@pytest.mark.parametrize("name", ["q8_0_tiny", "q4_0_7b", "q4_k_ffn_up", "iq1_m_dense"])
+@pytest.mark.parametrize("name", ["q8_0_tiny", "q4_0_7b", "q4_k_ffn_up", "iq1_m_dense", "q6_k_ffn_down"])
 def test_dense_block_workload_full_size(name):
     pb = synth.workload(name)
     M, N, K = pb.M, pb.N, pb.K

@@ -13,7 +13,8 @@ from block_quantized_int8_q8_gb300 import api, synth
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-3
-BLOCK_TYPES = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M]
+BLOCK_TYPES = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M, synth.Q6_K]
+PARTIAL_TYPES = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M, synth.W8A8]   # the general kernel's types
 DEV = "cuda"
 
 
@@ -108,7 +109,7 @@ def test_block_gemm_matches_oracle(wtype, shape):
     assert _rel_err(out, ref) <= TOL
 
 
-@pytest.mark.parametrize("wtype", BLOCK_TYPES + [synth.W8A8])
+@pytest.mark.parametrize("wtype", PARTIAL_TYPES)
 @pytest.mark.parametrize("shape", [(3, 5, 256), (131, 200, 512)])
 def test_debug_partials_bit_exact(wtype, shape):
     M, N, K = shape
@@ -178,7 +179,7 @@ def test_quantize_then_gemm_end_to_end(wtype):
 
 
 # ---------------------------------------------------------------------------------------- MoE
-@pytest.mark.parametrize("wtype", [synth.IQ1_M, synth.Q4_K, synth.Q8_0])
+@pytest.mark.parametrize("wtype", [synth.IQ1_M, synth.Q4_K, synth.Q8_0, synth.Q6_K])
 @pytest.mark.parametrize("M,E,slots,N,K", [(24, 6, 3, 130, 256), (300, 16, 4, 256, 512)])
 def test_gemm_id_matches_oracle(wtype, M, E, slots, N, K):
     pb = synth.make_problem(wtype, M, N, K, seed=51 + M + wtype, experts=E, slots=slots)
