@@ -20,6 +20,7 @@ DEVERR_TIMEOUT, DEVERR_EXPERT_ID, DEVERR_DUP_EXPERT = 1, 2, 4
 #: every symbol include/mmq.h declares
 EXPORTS = ("mmq_status_string", "mmq_last_cuda_error", "mmq_q8_1_bytes", "mmq_weight_bytes", "mmq_w8a8_act_bytes", "mmq_quantize_q8_1",
            "mmq_gemm", "mmq_gemm_id_workspace_bytes", "mmq_gemm_id", "mmq_gemm_debug_partials",
+           "mmq_gemm_debug_block_sums",
            "mmq_read_device_errors", "mmq_gemm_id_noalloc", "mmq_q8_1_prepare")
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -66,6 +67,8 @@ def load():
     lib.mmq_gemm_id.restype = I
     lib.mmq_gemm_debug_partials.argtypes = [I, P, P, P, I64, I64, I64, P]
     lib.mmq_gemm_debug_partials.restype = I
+    lib.mmq_gemm_debug_block_sums.argtypes = [I, P, P, P, I64, I64, I64, P]
+    lib.mmq_gemm_debug_block_sums.restype = I
     lib.mmq_gemm_id_noalloc.argtypes = [I, P, I, P, P, I, P, I64, I64, I64, P]
     lib.mmq_gemm_id_noalloc.restype = I
     lib.mmq_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), P]
@@ -185,6 +188,15 @@ def gemm_debug_partials(wtype: int, W: torch.Tensor, Xq: torch.Tensor, M: int, N
     out = torch.empty((M, N, K // G), dtype=torch.int32, device=W.device)
     _check(load().mmq_gemm_debug_partials(wtype, _ptr(W), _ptr(Xq), _ptr(out), M, N, K, _stream(stream)),
            "mmq_gemm_debug_partials")
+    return out
+
+
+def gemm_debug_block_sums(wtype: int, W: torch.Tensor, Xq: torch.Tensor, M: int, N: int, K: int,
+                          stream=None) -> torch.Tensor:
+    """The TMA-fed kernel's exact 32-k block accumulators (mmq_gemm_debug_block_sums): int32 [M, N, K/32]."""
+    out = torch.empty((M, N, K // 32), dtype=torch.int32, device=W.device)
+    _check(load().mmq_gemm_debug_block_sums(wtype, _ptr(W), _ptr(Xq), _ptr(out), M, N, K, _stream(stream)),
+           "mmq_gemm_debug_block_sums")
     return out
 
 

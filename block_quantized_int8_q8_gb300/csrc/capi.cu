@@ -228,6 +228,32 @@ mmq_status mmq_gemm_debug_partials(mmq_type wtype, const void* W, const void* Xq
     return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm_debug_partials");
 }
 
+mmq_status mmq_gemm_debug_block_sums(mmq_type wtype, const void* W, const void* Xq, int32_t* sums, int64_t M,
+                                     int64_t N, int64_t K, mmq_stream_t stream) {
+    if (!known_type(wtype)) return MMQ_ERR_INVALID_ARG;
+    mmq_status st = check_shape(wtype, M, N, K);
+    if (st != MMQ_OK) return st;
+    if (!block_type(wtype) || !tma_gemm_supported((int)wtype, K)) return MMQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return MMQ_OK;
+    if (!W || !Xq || !sums) return MMQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(Xq) || !aligned16(sums)) return MMQ_ERR_ALIGN;
+    const Q81Layout L = q81_layout(M, K);
+    const uint8_t* xb = static_cast<const uint8_t*>(Xq);
+    TmaGemmArgs a{};
+    a.W = W;
+    a.xh = xb + L.h;
+    a.dT = reinterpret_cast<const float*>(xb + L.dT);
+    a.sT = reinterpret_cast<const float*>(xb + L.sT);
+    a.out = reinterpret_cast<float*>(sums);
+    a.w_row_bytes = weight_row_bytes(wtype, K);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.Mp = L.Mp;
+    const cudaError_t e = run_gemm_tma((int)wtype, a, reinterpret_cast<cudaStream_t>(stream), true);
+    return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm_debug_block_sums");
+}
+
 size_t mmq_gemm_id_workspace_bytes(int64_t M, int64_t K, int n_slots, int n_experts) {
     if (M < 0 || K < 0 || n_slots <= 0 || n_experts <= 0) return 0;
     return id_layout(M, K, n_slots, n_experts).total;

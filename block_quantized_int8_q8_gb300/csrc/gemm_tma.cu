@@ -66,7 +66,7 @@ int moe_kparts(int wt, long long K) {
 }
 
 template <int WT>
-cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
+cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
     using L = tma::Smem<WT>;
     constexpr int U = tma::Geom<WT>::U;
     CUtensorMap tm_raw, tm_b, tm_xd, tm_xs;
@@ -104,15 +104,24 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream) {
     }
     auto kern = tma::mmq_gemm_tma_kernel<WT, false>;
     auto kern_moe = tma::mmq_gemm_tma_kernel<WT, true>;
+    auto kern_dbg = tma::mmq_gemm_tma_kernel<WT, false, true>;
     static bool configured = false;       // per instantiation; the attribute is per function
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern_moe, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern_dbg, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const long long ntn = (a.N + BM - 1) / BM;
+    if (dbg) {                              // block sums: one CTA per tile, whole K range
+        const long long T = ntn * ((a.M + BN - 1) / BN);
+        kern_dbg<<<(unsigned)T, tma::Warps<WT>::kThreads, L::alloc, stream>>>(
+            tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)T, 0, tma::MoeTiles{});
+        return cudaGetLastError();
+    }
     if (a.work != nullptr) {                // MoE: one CTA per (work item, weight-row tile) + tail parts
         const tma::MoeTiles moe{a.work, a.nwork, a.gstart, a.rowlist, sm_count(), moe_kparts(WT, a.K)};
         const long long ctas = ntn * a.max_work + moe.sms;
@@ -283,13 +292,13 @@ bool tma_gemm_supported(int wt, long long K) {
     return (wt == WT_Q8_0 || wt == WT_Q4_0 || wt == WT_Q4_K || wt == WT_Q6_K) && K % 256 == 0;
 }
 
-cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s) {
+cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s, bool block_sums) {
     switch (wt) {
-        case WT_Q8_0: return launch<WT_Q8_0>(a, s);
-        case WT_Q4_0: return launch<WT_Q4_0>(a, s);
-        case WT_Q4_K: return launch<WT_Q4_K>(a, s);
-        case WT_IQ1_M: return launch<WT_IQ1_M>(a, s);
-        case WT_Q6_K: return launch<WT_Q6_K>(a, s);
+        case WT_Q8_0: return launch<WT_Q8_0>(a, s, block_sums);
+        case WT_Q4_0: return launch<WT_Q4_0>(a, s, block_sums);
+        case WT_Q4_K: return launch<WT_Q4_K>(a, s, block_sums);
+        case WT_IQ1_M: return launch<WT_IQ1_M>(a, s, block_sums);
+        case WT_Q6_K: return launch<WT_Q6_K>(a, s, block_sums);
     }
     return cudaErrorInvalidValue;
 }

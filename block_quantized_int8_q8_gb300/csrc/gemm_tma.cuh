@@ -342,7 +342,10 @@ __host__ __device__ __forceinline__ int tail_split(int T, int sms, int kparts, i
     return lg;
 }
 
-template <int WT, bool MOE>
+// DBG: instead of the rescale, the epilogue stores every 32-k block's exact integer accumulator (the weights'
+// integer sub-scales folded in, as the converters fold them) to int32 [M][N][K/32] at `out`; dense, whole
+// K range per CTA.
+template <int WT, bool MOE, bool DBG = false>
 __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
@@ -553,26 +556,44 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
                 uint32_t(&cur)[16] = (k & 1) ? vb : va;
                 uint32_t(&nxt)[16] = (k & 1) ? va : vb;
                 if (kn < 4) tmem_ld_16x256b_x4(tacc + (kn >> 1) * BN + ((uint32_t)(16 * (kn & 1)) << 16), nxt);
-                if (h == 0) {                                          // token scales of block i
+                if constexpr (DBG) {
+                    int* dbg = reinterpret_cast<int*>(out);
+                    const long long nb = K / 32, bglob = 2 * (s + s0) + i;
 #pragma unroll
-                    for (int jj = 0; jj < 4; jj++) {
-                        const uint32_t col = EPI_COLS * cq + 8 * jj + 2 * tc;
-                        const float2 x = ld_shared_f2(scs + L::xd_off + 4 * (i * BN + col));
-                        xd2[jj] = f2_pack(x.x, x.y);
-                        if constexpr (L::kMin) {
-                            const float2 y = ld_shared_f2(scs + L::xs_off + 4 * (i * BN + col));
-                            xs2[jj] = f2_pack(y.x, y.y);
+                    for (int e = 0; e < 2; e++) {
+                        const int n = n0 + 32 * q + 16 * h + 8 * e + tq;
+#pragma unroll
+                        for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+                            for (int c2 = 0; c2 < 2; c2++) {
+                                const int col = EPI_COLS * cq + 8 * jj + 2 * tc + c2;
+                                if (n < N && col < mvalid)
+                                    dbg[((long long)(m0 + col) * N + n) * nb + bglob] =
+                                        __float2int_rn(__uint_as_float(cur[4 * jj + 2 * e + c2]));
+                            }
+                    }
+                } else {
+                    if (h == 0) {                                      // token scales of block i
+#pragma unroll
+                        for (int jj = 0; jj < 4; jj++) {
+                            const uint32_t col = EPI_COLS * cq + 8 * jj + 2 * tc;
+                            const float2 x = ld_shared_f2(scs + L::xd_off + 4 * (i * BN + col));
+                            xd2[jj] = f2_pack(x.x, x.y);
+                            if constexpr (L::kMin) {
+                                const float2 y = ld_shared_f2(scs + L::xs_off + 4 * (i * BN + col));
+                                xs2[jj] = f2_pack(y.x, y.y);
+                            }
                         }
                     }
-                }
-                float w[2], mn[2] = {0.f, 0.f};
+                    float w[2], mn[2] = {0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const int row = 32 * q + 16 * h + 8 * e + tq;
-                    w[e] = ld_shared_f32(scs + L::wd_off + 4 * (i * BM + row));
-                    if constexpr (L::kMin) mn[e] = ld_shared_f32(scs + L::wmn_off + 4 * (i * BM + row));
+                    for (int e = 0; e < 2; e++) {
+                        const int row = 32 * q + 16 * h + 8 * e + tq;
+                        w[e] = ld_shared_f32(scs + L::wd_off + 4 * (i * BM + row));
+                        if constexpr (L::kMin) mn[e] = ld_shared_f32(scs + L::wmn_off + 4 * (i * BM + row));
+                    }
+                    rescale_half<L::kMin>(acc[h], cur, xd2, xs2, w, mn);
                 }
-                rescale_half<L::kMin>(acc[h], cur, xd2, xs2, w, mn);
                 if (kn < 4) tmem_ld_wait(nxt);
                 if (kn == 3) {
                     tc_fence_before();          // every TMEM read of this stage buffer is complete
@@ -585,6 +606,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         }
         // ---- store: rows n0 + 32q + 16h + 8e + tq, token columns 32cq + 8j + 2tc + {0, 1} below mvalid;
         // output row of a column: m0 + column (dense) or its rowlist entry (MoE)
+      if constexpr (!DBG) {
         int orow[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) {
@@ -615,6 +637,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
                 }
             }
         }
+      }
     }
 
     // ---- teardown

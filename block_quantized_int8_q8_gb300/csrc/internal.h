@@ -41,7 +41,9 @@ struct TmaGemmArgs {
     int max_work = 0;
 };
 bool tma_gemm_supported(int wt, long long K);
-cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s);
+// block_sums: instead of the product, int32 [M][N][K/32] of every 32-k block's exact integer accumulator
+// (dense only; `out` then points at the int32 array).
+cudaError_t run_gemm_tma(int wt, const TmaGemmArgs& a, cudaStream_t s, bool block_sums = false);
 // MoE operand gather (gemm_tma.cu): the fp16 codes and block scales of each work item's token rows,
 // copied to rows gstart[w] .. gstart[w] + count - 1 of xg [Rg][K] / dTg, sTg [K/32][Rg]; gstart[w] is
 // the 4-aligned prefix sum of the preceding items' counts.  Rg >= M*slots + 3*max_work, Rg % 4 == 0.

@@ -145,6 +145,18 @@ mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out,
                     int64_t M, int64_t N, int64_t K, mmq_stream_t stream);
 
 /*
+ * mmq_gemm_debug_block_sums -- the production (TMA-fed) kernel's exact integer accumulators.
+ * Instead of the product, writes sums[m][n][b] (int32 [M][N][K/32]) = the 32-k block dot of token row m
+ * and weight row n with the weights' integer sub-scale factors folded in, as the kernel's converters fold
+ * them: Q8_0 q, Q4_0 code-8, Q4_K sc_b*code, IQ1_M (2s+1)*(8g+-1) per 16 values, Q6_K sc_h*(code-32) per
+ * 16 values ("08 · R1", §2.1: the in-block integer dot is exact; §2.2 for the K-quant sub-scales).  For
+ * parity checks of the tensor-core path, bit for bit; block types on shapes the TMA-fed kernel takes
+ * (K % 256 == 0; IQ1_M K % 1024 == 0), else MMQ_ERR_UNSUPPORTED.  sums is caller-owned, 16-byte aligned.
+ */
+mmq_status mmq_gemm_debug_block_sums(mmq_type wtype, const void* W, const void* Xq, int32_t* sums,
+                                     int64_t M, int64_t N, int64_t K, mmq_stream_t stream);
+
+/*
  * mmq_gemm_id -- MoE MUL_MAT_ID ("CUDA: add IQ1_M to MMQ", PR description): each token times each of
  * its routed experts.
  * W          : n_experts expert weight matrices of type wtype (block types only), back to back, each

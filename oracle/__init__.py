@@ -11,6 +11,9 @@ Functions and the passages they follow (page title, section):
                   "CUDA: add IQ1_M to MMQ", Design (IQ1_M fold 8g±1, per-16 scale d(2s+1)/8);
                   "08 · R1", §2.2 (q6_K: 6-bit grid minus 32, int8 scales per 16 elements)
   partials        "08 · R1", §2.1 (exact in-block int32 dot)
+  block_sums      the same 32-k block dot on the weights with their integer sub-scales folded in
+                  ("08 · R1" §2.2 per-sub-block scales, q6_K's two scaled dots; "CUDA: add IQ1_M to
+                  MMQ", Design: d(2s+1) per 16 values)
   gemm/gemm_rows  "When the Product Won't Collapse: A Negative Result on int8 Tensor-Core MMQ", §2
                   (blockwise contraction) with the §3.2 per-block correction of "08 · R1"
   w8a8            "INT8 W8A8 GEMM — Prefill", §1-§2 (full-K int32, scale epilogue, bf16)
@@ -61,6 +64,7 @@ def _load():
         lib.oracle_quantize_q8_1.argtypes = [P, I64, I64, P, P, P]
         lib.oracle_decode.argtypes = [ctypes.c_int, P, I64, I64, P, P, P]
         lib.oracle_partials.argtypes = [ctypes.c_int, P, P, I64, I64, I64, P]
+        lib.oracle_block_sums.argtypes = [ctypes.c_int, P, P, I64, I64, I64, P]
         lib.oracle_gemm.argtypes = [ctypes.c_int, P, P, P, P, I64, I64, I64, P]
         lib.oracle_gemm_rows.argtypes = [ctypes.c_int, P, P, P, P, I64, I64, I64, P, I64, P]
         lib.oracle_w8a8.argtypes = [P, P, P, P, I64, I64, I64, P]
@@ -122,6 +126,17 @@ def partials(wtype: int, xq: np.ndarray, wq: np.ndarray) -> np.ndarray:
     P = np.empty((M, N, K // group_size(wtype)), np.int32)
     _check(_load().oracle_partials(wtype, _p(xq), _p(wq), M, N, K, _p(P)))
     return P
+
+
+def block_sums(wtype: int, W: np.ndarray, xq: np.ndarray, N: int) -> np.ndarray:
+    """Exact 32-k block sums with the weights' integer sub-scale factors folded in: int32 [M, N, K/32]
+    (Q4_K: sc_b; IQ1_M: (2s+1) per 16; q6_K: sc per 16; Q8_0 / Q4_0: none)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    M, K = xq.shape
+    A = np.empty((M, N, K // 32), np.int32)
+    _check(_load().oracle_block_sums(wtype, _p(W), _p(xq), M, N, K, _p(A)))
+    return A
 
 
 def gemm(wtype: int, W: np.ndarray, q: np.ndarray, d: np.ndarray, s: np.ndarray, N: int) -> np.ndarray:

@@ -306,6 +306,59 @@ int oracle_partials(int wtype, const int8_t* xq, const int8_t* wq, int64_t M, in
     return 0;
 }
 
+/* ---------------------------------------------------------------- folded 32-k block sums */
+/*
+ * Integer factor of each group's weight scale that is an exact integer: Q4_K's 6-bit sc_b per 32
+ * ([R1] §2.2 (d*s) per sub-block), IQ1_M's (2s+1) per 16 ([IQ] Design: d(2s+1) per 16 values), q6_K's
+ * int8 sc_h per 16 ([R1] §2.2).  Q8_0 / Q4_0 have none (factor 1).
+ */
+static void decode_row_int_scale(int wtype, const uint8_t* row, int64_t K, int32_t* isc) {
+    if (wtype == OR_Q4_K) {
+        for (int64_t sb = 0; sb < K / 256; sb++)
+            for (int j = 0; j < 8; j++) isc[sb * 8 + j] = (int32_t)bits_le(row + sb * 144 + 4, 6u * (unsigned)j, 6);
+    } else if (wtype == OR_IQ1_M) {
+        for (int64_t sb = 0; sb < K / 256; sb++)
+            for (int h = 0; h < 16; h++)
+                isc[sb * 16 + h] = (int32_t)(2u * bits_le(row + sb * 76 + 68, 3u * (unsigned)h, 3) + 1u);
+    } else if (wtype == OR_Q6_K) {
+        for (int64_t sb = 0; sb < K / 256; sb++)
+            for (int h = 0; h < 16; h++) isc[sb * 16 + h] = (int32_t)(int8_t)row[sb * 224 + h];
+    } else {
+        for (int64_t g = 0; g < K / 32; g++) isc[g] = 1;
+    }
+}
+
+/*
+ * A[m][n][b] = sum over k in 32-block b of xq[m][k] * wq[n][k] * isc[n][group(k)]: the exact integer
+ * block sum with each group's integer scale factor folded in (the 32-k block dot of [R1] §2.1 on the
+ * folded operand; for IQ1_M and q6_K the sum of the block's two per-16 dots, each times its factor).
+ */
+int oracle_block_sums(int wtype, const uint8_t* W, const int8_t* xq, int64_t M, int64_t N, int64_t K,
+                      int32_t* A) {
+    if (!block_type(wtype) || check_k(wtype, K)) return 1;
+    const int64_t G = group_size(wtype), nb = K / 32;
+    const int64_t ngi = (wtype == OR_Q8_0 || wtype == OR_Q4_0) ? K / 32 : K / G;
+    int8_t* wq = (int8_t*)malloc((size_t)(N * K));
+    float* wsc = (float*)malloc((size_t)(N * (K / G)) * sizeof(float));
+    float* wmin = (float*)malloc((size_t)(N * nb) * sizeof(float));
+    int32_t* isc = (int32_t*)malloc((size_t)(N * ngi) * sizeof(int32_t));
+    if (!wq || !wsc || !wmin || !isc) { free(wq); free(wsc); free(wmin); free(isc); return 2; }
+    oracle_decode(wtype, W, N, K, wq, wsc, wmin);
+    for (int64_t n = 0; n < N; n++) decode_row_int_scale(wtype, W + n * row_bytes(wtype, K), K, isc + n * ngi);
+    const int64_t gi = K / ngi;                           /* values per integer-scale group */
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++)
+            for (int64_t b = 0; b < nb; b++) {
+                int64_t acc = 0;
+                for (int64_t k = b * 32; k < b * 32 + 32; k++)
+                    acc += (int64_t)xq[m * K + k] * (int64_t)wq[n * K + k] * (int64_t)isc[n * ngi + k / gi];
+                A[(m * N + n) * nb + b] = (int32_t)acc;
+            }
+    free(wq); free(wsc); free(wmin); free(isc);
+    return 0;
+}
+
 /* ---------------------------------------------------------------- blockwise product for one row pair */
 /*
  * [NR] §2: out[m,n] = sum_kb (xs[m,kb] * wd[n,kb]) * sum_{k in kb} xq[m,k] * wq[n,k]

@@ -126,6 +126,38 @@ def test_debug_partials_bit_exact(wtype, shape):
     assert np.array_equal(P, ref)
 
 
+@pytest.mark.parametrize("wtype", BLOCK_TYPES)
+@pytest.mark.parametrize("shape", [(3, 5, 1024), (131, 200, 2048), (257, 130, 1024)])
+def test_tma_block_sums_bit_exact(wtype, shape):
+    # the production kernel's integer accumulators, sub-scales folded in, bit for bit
+    M, N, K = shape
+    pb = synth.make_problem(wtype, M, N, K, seed=23 + M + wtype)
+    q, d, s, xq = _oracle_acts(pb)
+    A = api.gemm_debug_block_sums(wtype, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    assert api.read_device_errors() == 0
+    assert np.array_equal(A, oracle.block_sums(wtype, pb.W, q, N))
+
+
+def test_tma_block_sums_exact_at_the_bounds():
+    # q6_K with |q - 32| = 32 and sc = -128 everywhere against activation codes of +-127: every block sum
+    # is 32 * 4096 * 127 in magnitude, the largest the folded operands can produce (< 2^24)
+    M, N, K = 4, 130, 1024
+    pb = synth.make_problem(synth.Q6_K, M, N, K, seed=29)
+    pb.fields.code[...] = 0
+    pb.fields.sc[...] = -128
+    W = synth.pack(synth.Q6_K, pb.fields)
+    q = np.where(np.arange(M * K).reshape(M, K) % 3 == 0, -127, 127).astype(np.int8)
+    q[0] = 127                         # rows 0 and 1: every block sum at +-32 * 4096 * 127
+    q[1] = -127
+    d = np.full((M, K // 32), 0.01, np.float32)
+    s = (d * q.reshape(M, K // 32, 32).sum(-1)).astype(np.float32)
+    xq = api.pack_q8_1(torch.from_numpy(q), torch.from_numpy(d), torch.from_numpy(s)).to(DEV)
+    A = api.gemm_debug_block_sums(synth.Q6_K, _dev(W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    ref = oracle.block_sums(synth.Q6_K, W, q, N)
+    assert np.abs(ref).max() == 32 * 4096 * 127
+    assert np.array_equal(A, ref)
+
+
 def test_partials_exact_at_the_block_bound():
     # every product at its maximum magnitude: block dots of +-32*127*127 must come out exact
     M, N, K = 130, 130, 512

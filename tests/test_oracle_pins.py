@@ -253,6 +253,30 @@ def test_partials_brute_force(wtype):
                 assert P[m, n, gi] == ref
 
 
+@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M, synth.Q6_K])
+def test_block_sums_brute_force_from_generator_fields(wtype):
+    # the folded 32-k block sums computed in int64 straight from the drawn fields (no oracle decoder)
+    g = np.random.default_rng(60 + wtype)
+    M, N, K = 3, 5, 512
+    f = synth.draw_fields(g, wtype, N, K)
+    W = synth.pack(wtype, f)
+    xq = g.integers(-127, 128, size=(M, K)).astype(np.int8)
+    if wtype == synth.Q8_0:
+        wint = f.q.astype(np.int64)
+    elif wtype == synth.Q4_0:
+        wint = f.code.astype(np.int64) - 8
+    elif wtype == synth.Q4_K:
+        wint = np.repeat(f.sc.astype(np.int64), 32, 1) * f.code
+    elif wtype == synth.IQ1_M:
+        fold = 8 * f.g.astype(np.int64) + np.where(np.repeat(f.neg, 8, 1) == 1, -1, 1)
+        wint = np.repeat(2 * f.s.astype(np.int64) + 1, 16, 1) * fold
+    else:
+        wint = np.repeat(f.sc.astype(np.int64), 16, 1) * (f.code.astype(np.int64) - 32)
+    ref = np.einsum("mbk,nbk->mnb", xq.astype(np.int64).reshape(M, K // 32, 32), wint.reshape(N, K // 32, 32))
+    A = oracle.block_sums(wtype, W, xq, N)
+    assert np.array_equal(A.astype(np.int64), ref)
+
+
 def test_partial_bounds_from_pages():
     bounds = dict(line.split() for line in _golden_ints("bounds.txt"))
     # IQ1_M per-16 extreme: q = 127 against the largest fold value 9 everywhere
