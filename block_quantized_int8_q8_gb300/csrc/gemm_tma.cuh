@@ -231,7 +231,9 @@ __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t raw) {
     }
     const uint32_t at = c.sb + L::a_off + slot * Ring<WT>::kAStage;
     const uint32_t scs = c.sb + L::sc_off + ss * L::sc_slot;
-#pragma unroll 1
+    // both rows of a 2-row thread in one unrolled body: the second row's raw loads and unpack overlap the
+    // first's (measured +9 % on Q4_0, +4 % on Q4_K against one row at a time)
+#pragma unroll
     for (int rr = 0; rr < Warps<WT>::kRowsPerConv; rr++) {
         const int row = c.pt + rr * Warps<WT>::kConv * 32;
         RawA r;
