@@ -9,6 +9,7 @@
 #include "../../include/mmq.h"
 #include "gemm.cuh"
 #include "internal.h"
+#include "gemv.h"
 
 using namespace mmq;
 
@@ -183,6 +184,12 @@ mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out, in
     if (!W || !Xq || !out) return MMQ_ERR_INVALID_ARG;
     if (!aligned16(W) || !aligned16(Xq) || !aligned16(out)) return MMQ_ERR_ALIGN;
     if (wtype == MMQ_W8A8 && (((M * K) & 3) || ((N * K) & 3))) return MMQ_ERR_ALIGN;
+    if (block_type(wtype) && M <= mmvq_max_m((int)wtype)) {
+        // a few tokens: the matrix-vector kernel (gemv.cu), weights read once at memory speed
+        const cudaError_t e = run_gemv((int)wtype, W, weight_row_bytes(wtype, K), Xq, static_cast<float*>(out), M, N,
+                                       K, reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm");
+    }
     if (block_type(wtype) && tma_gemm_supported((int)wtype, K)) {
         // the TMA-fed kernel (gemm_tma.cuh); the general kernel covers the remaining shapes
         const Q81Layout L = q81_layout(M, K);

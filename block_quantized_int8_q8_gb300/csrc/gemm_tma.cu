@@ -58,11 +58,11 @@ int sm_count() {
     return counts[dev];
 }
 
-// Largest K split (4, 2 or 1) of a MoE tail tile whose parts hold whole raw super-stages.
+// Largest K split (4, 2 or 1) of a MoE tail tile: parts are cut at raw super-stage boundaries, so a tile
+// splits into at most as many parts as it has super-stages.
 int moe_kparts(int wt, long long K) {
-    const long long nst = K / BK;
-    const int ss = wt == WT_IQ1_M ? tma::Geom<WT_IQ1_M>::SS : tma::Geom<WT_Q4_0>::SS;
-    return nst % (4 * ss) == 0 ? 4 : (nst % (2 * ss) == 0 ? 2 : 1);
+    const long long nsup = K / BK / (wt == WT_IQ1_M ? tma::Geom<WT_IQ1_M>::SS : tma::Geom<WT_Q4_0>::SS);
+    return nsup >= 4 ? 4 : (nsup >= 2 ? 2 : 1);
 }
 
 template <int WT>
@@ -137,13 +137,14 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
     const int sms = sm_count();
     const long long nst = a.K / BK;
     constexpr int SS = tma::Geom<WT>::SS;
+    const long long nsup = nst / SS;                           // parts are cut at super-stage boundaries
     long long split_rows = 0;
     int lgp = 1;
-    if (sms > 0 && 2 * T <= sms && nst % (2 * SS) == 0) {
+    if (sms > 0 && 2 * T <= sms && nsup >= 2) {
         lgp = 1;
-        while (lgp < 4 && (T << (lgp + 1)) <= sms && nst % ((long long)SS << (lgp + 1)) == 0) lgp++;
+        while (lgp < 4 && (T << (lgp + 1)) <= sms && (2ll << lgp) <= nsup) lgp++;
         split_rows = ntm;
-    } else if (sms > 0 && T > sms && nst % (2 * SS) == 0) {
+    } else if (sms > 0 && T > sms && nsup >= 2) {
         const long long r = T - (T - 1) / sms * sms;          // tiles in the last wave
         if (2 * r <= sms) split_rows = (r + ntn - 1) / ntn;
         if (split_rows >= ntm) split_rows = 0;

@@ -394,8 +394,14 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         wrow = n0;
         mvalid = M - m0;
     }
-    const int nstages = part < 0 ? K / BK : (K / BK) >> lgparts;   // stages of this CTA's K range
-    const int s0 = part < 0 ? 0 : part * nstages;
+    // K range of this CTA: all stages, or part `part` of 2^lgparts, cut at raw super-stage boundaries
+    int nstages = K / BK, s0 = 0;
+    if (part >= 0) {
+        const int nsup = K / BK / SS;
+        const int t0 = (part * nsup) >> lgparts, t1 = ((part + 1) * nsup) >> lgparts;
+        s0 = t0 * SS;
+        nstages = (t1 - t0) * SS;
+    }
 
     Ctx c;
     c.sb = smem_u32(smem);

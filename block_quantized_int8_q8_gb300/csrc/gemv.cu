@@ -1,0 +1,238 @@
+// gemv.cu -- the few-token path (M <= 8) of the block types: a matrix-vector kernel that reads every weight
+// byte once at memory speed instead of filling 128-token tensor-core tiles ("CUDA: add IQ1_M to MMQ":
+// small batches run on the matrix-vector path; the MMQ tiles win from ~100 tokens on).
+//
+// One warp per weight row.  The row is walked in chunks of 32 blocks of 32 values, one block per lane:
+// the warp stages the chunk's raw bytes in shared memory with coalesced 4-byte loads, each lane decodes
+// its block to int8 words, forms the exact int32 block dot per token with dp4a ("08 · R1 — int8 MMQ
+// prefill GEMM", §2.1: the in-block integer dot is exact), and its f32 term u = (xd * wsc) * I
+// (Q4_K: minus dmin*m_b * s; IQ1_M and q6_K: one term per 16-value half).  Lane m then adds the chunk's
+// terms in block order into token m's running sum ("A Negative Result on int8 Tensor-Core MMQ", §2: the
+// blockwise contraction).  Every product and sum is a separate round-to-nearest step in the order written,
+// so the output is bit-identical to the blockwise definition computed in that order.
+#include <cstdint>
+#include <cuda_fp16.h>
+#include "gemv.h"
+#include "gemm.cuh"
+#include "mmq_device.cuh"
+
+namespace mmq {
+namespace gemv {
+
+constexpr int WARPS = 8;                 // rows in flight per CTA
+constexpr int CHUNK = 32;                // 32-value blocks per chunk (one per lane)
+constexpr int STAGE_WORDS = 1088 / 4 + 1;   // largest chunk (Q8_0: 32 x 34 B) plus one word of overrun
+constexpr int STAGE_WORDS_16 = (STAGE_WORDS + 3) / 4 * 4;   // ring slots on 16-byte boundaries
+
+// Raw bytes of one chunk (32 blocks = 1024 values) per type.
+__host__ __device__ constexpr int chunk_bytes(int wt) {
+    return wt == WT_Q8_0 ? 32 * 34 : wt == WT_Q4_0 ? 32 * 18 : wt == WT_Q4_K ? 4 * 144 : wt == WT_IQ1_M ? 4 * 76 : 4 * 224;
+}
+__host__ __device__ constexpr bool per16(int wt) { return wt == WT_IQ1_M || wt == WT_Q6_K; }
+
+// 32-bit word at byte offset o of the staged chunk (any alignment).
+__device__ __forceinline__ uint32_t st_word(const uint32_t* st, int o) {
+    return __funnelshift_r(st[o >> 2], st[(o >> 2) + 1], 8 * (o & 3));
+}
+__device__ __forceinline__ float st_half(const uint32_t* st, int o) {
+    return __half2float(__ushort_as_half((unsigned short)(st_word(st, o) & 0xFFFFu)));
+}
+// Field [pos, pos + width) of a little-endian bit stream starting at byte o (width <= 8).
+__device__ __forceinline__ uint32_t st_field(const uint32_t* st, int o, int pos, int width) {
+    return (st_word(st, o + (pos >> 3)) >> (pos & 7)) & ((1u << width) - 1u);
+}
+
+// Decode block j (0..31) of the staged chunk: 8 words of int8 values in k order and the scale factors of
+// the blockwise definition (per 32 values, or per 16-value half: wsc[0], wsc[1]).
+template <int WT>
+__device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t (&w)[8], float (&wsc)[2],
+                                             float& wmin) {
+    wmin = 0.f;
+    if constexpr (WT == WT_Q8_0) {                 // f16 d | int8 q[32]
+        const int o = 34 * j;
+        wsc[0] = wsc[1] = st_half(st, o);
+#pragma unroll
+        for (int k = 0; k < 8; k++) w[k] = st_word(st, o + 2 + 4 * k);
+    } else if constexpr (WT == WT_Q4_0) {          // f16 d | byte i = code i (low) | code i+16 (high)
+        const int o = 18 * j;
+        wsc[0] = wsc[1] = st_half(st, o);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint32_t nw = st_word(st, o + 2 + 4 * k);
+            w[k] = __vsub4(nw & 0x0F0F0F0Fu, 0x08080808u);            // code - 8
+            w[4 + k] = __vsub4((nw >> 4) & 0x0F0F0F0Fu, 0x08080808u);
+        }
+    } else if constexpr (WT == WT_Q4_K) {          // f16 d | f16 dmin | 12 B six-bit sc, m | 128 B codes
+        const int o = 144 * (j >> 3), sb = j & 7;
+        const float d = st_half(st, o), dmin = st_half(st, o + 2);
+        wsc[0] = wsc[1] = __fmul_rn(d, (float)st_field(st, o + 4, 6 * sb, 6));
+        wmin = __fmul_rn(dmin, (float)st_field(st, o + 4, 6 * (8 + sb), 6));
+        const int co = o + 16 + 32 * (sb >> 1), sh = 4 * (sb & 1);  // sub-block 2p (low) / 2p+1 (high nibbles)
+#pragma unroll
+        for (int k = 0; k < 8; k++) w[k] = (st_word(st, co + 4 * k) >> sh) & 0x0F0F0F0Fu;
+    } else if constexpr (WT == WT_IQ1_M) {         // 64 B codes | 4 B signs | 6 B three-bit s | f16 d
+        const int o = 76 * (j >> 3), sb = j & 7;
+        const float d = st_half(st, o + 74);
+#pragma unroll
+        for (int h = 0; h < 2; h++)
+            wsc[h] = __fmul_rn(__fmul_rn(d, (float)(2u * st_field(st, o + 68, 3 * (2 * sb + h), 3) + 1u)), 0.125f);
+        const uint32_t signs = st_word(st, o + 64) >> (4 * sb);        // one bit per 8 values
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const uint32_t cb = st_word(st, o + 8 * sb + k) & 0xFFu;    // codes of values 4k..4k+3
+            const uint32_t c = (cb & 3u) | ((cb & 0x0Cu) << 6) | ((cb & 0x30u) << 12) | ((cb & 0xC0u) << 18);
+            // 8 * (code - 1) + (+1 | -1), per byte: 8 * code + (-7 | -9)
+            w[k] = __vadd4(c << 3, ((signs >> (k >> 1)) & 1u) ? 0xF7F7F7F7u : 0xF9F9F9F9u);
+        }
+    } else {                                        // q6_K: int8 sc[16] | f16 d | pad | four 48 B records
+        const int o = 224 * (j >> 3), sb = j & 7;
+        const float d = st_half(st, o + 16);
+#pragma unroll
+        for (int h = 0; h < 2; h++) wsc[h] = __fmul_rn(d, (float)(int8_t)(st_word(st, o + 2 * sb + h) & 0xFFu));
+        const int rec = o + 32 + 48 * (sb >> 1), hh = sb & 1;           // record of the 64-value stage
+#pragma unroll
+        for (int k = 0; k < 8; k++) {                                   // values 32hh + 4k .. + 3 of the stage
+            const uint32_t lo = (st_word(st, rec + 4 * k) >> (4 * hh)) & 0x0F0F0F0Fu;
+            const uint32_t hi = ((st_word(st, rec + 32 + 4 * (k & 3)) >> (2 * (2 * hh + (k >> 2)))) & 0x03030303u) << 4;
+            w[k] = __vsub4(lo | hi, 0x20202020u);                       // code - 32
+        }
+    }
+}
+
+// Grid-stride over weight rows, one row per warp at a time; MT tokens.  xq: int8 codes [MT][K];
+// xds: (d, s) [MT][K/32].  The row's chunks stream into a DEPTH-slot shared-memory ring with cp.async, so
+// DEPTH - 1 chunks of the weight stream are in flight while one is decoded.
+constexpr int DEPTH = 3;
+
+template <int WT, int MT>
+__global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restrict__ W, long long row_bytes,
+                                                        const int8_t* __restrict__ xq,
+                                                        const float2* __restrict__ xds, float* __restrict__ out,
+                                                        int N, int K) {
+    constexpr int TPB = per16(WT) ? 2 : 1;        // terms per block
+    __shared__ __align__(16) uint32_t stage[WARPS][DEPTH][STAGE_WORDS_16];
+    __shared__ float terms[WARPS][MT][TPB * CHUNK + 1];   // odd row pitch: the summing lanes' reads hit distinct banks
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = K / 32, nchunks = (nb + CHUNK - 1) / CHUNK;
+    const bool row16 = (row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(W) & 15) == 0;
+    for (long long n = (long long)blockIdx.x * WARPS + warp; n < N; n += (long long)gridDim.x * WARPS) {
+        const uint8_t* row = W + n * row_bytes;
+        // copy chunk c's raw words into ring slot c % DEPTH (one commit group per chunk, empty past the end)
+        // (16-byte copies that bypass L1 when the chunk allows it, so the weight stream does not evict the
+        // activations every row reads)
+        auto issue = [&](int c) {
+            if (c < nchunks) {
+                const int words = min(CHUNK, nb - c * CHUNK) * chunk_bytes(WT) / 128;   // whole words: K % 256 == 0
+                const uint8_t* src = row + (long long)c * chunk_bytes(WT);
+                const uint32_t dst = smem_u32(stage[warp][c % DEPTH]);
+                if (row16 && (words & 3) == 0) {
+                    for (int i = lane; i < words / 4; i += 32) cp_async_16(dst + 16 * i, src + 16 * i, 16);
+                } else {
+                    for (int i = lane; i < words; i += 32) cp_async_4(dst + 4 * i, src + 4 * i, 4);
+                }
+            }
+            cp_async_commit();
+        };
+        __syncwarp();                              // the previous row's last chunk is consumed
+#pragma unroll
+        for (int c = 0; c < DEPTH - 1; c++) issue(c);
+        float acc = 0.0f;                          // token `lane`'s running sum (lanes < MT)
+        for (int c = 0; c < nchunks; c++) {
+            issue(c + DEPTH - 1);                  // refills the slot chunk c - 1 used
+            cp_async_wait<DEPTH - 1>();            // this lane's copies of chunk c have landed
+            __syncwarp();                          // ... and every lane's
+            const uint32_t* st = stage[warp][c % DEPTH];
+            const int nblk = min(CHUNK, nb - c * CHUNK);
+            if (lane < nblk) {
+                const int b = c * CHUNK + lane;
+                int4 x0[MT], x1[MT];
+                float2 ds[MT];
+#pragma unroll
+                for (int m = 0; m < MT; m++) {     // every token's activation block in flight at once
+                    const int4* xp = reinterpret_cast<const int4*>(xq + (long long)m * K + 32 * b);
+                    x0[m] = __ldg(xp);
+                    x1[m] = __ldg(xp + 1);
+                    ds[m] = __ldg(xds + (long long)m * nb + b);
+                }
+                uint32_t w[8];
+                float wsc[2], wmin;
+                decode_block<WT>(st, lane, w, wsc, wmin);
+#pragma unroll
+                for (int m = 0; m < MT; m++) {
+                    int I0 = 0, I1 = 0;
+                    I0 = __dp4a((int)w[0], x0[m].x, I0);
+                    I0 = __dp4a((int)w[1], x0[m].y, I0);
+                    I0 = __dp4a((int)w[2], x0[m].z, I0);
+                    I0 = __dp4a((int)w[3], x0[m].w, I0);
+                    I1 = __dp4a((int)w[4], x1[m].x, I1);
+                    I1 = __dp4a((int)w[5], x1[m].y, I1);
+                    I1 = __dp4a((int)w[6], x1[m].z, I1);
+                    I1 = __dp4a((int)w[7], x1[m].w, I1);
+                    if constexpr (per16(WT)) {
+                        terms[warp][m][2 * lane] = __fmul_rn(__fmul_rn(ds[m].x, wsc[0]), (float)I0);
+                        terms[warp][m][2 * lane + 1] = __fmul_rn(__fmul_rn(ds[m].x, wsc[1]), (float)I1);
+                    } else {
+                        float u = __fmul_rn(__fmul_rn(ds[m].x, wsc[0]), (float)(I0 + I1));
+                        if constexpr (WT == WT_Q4_K) u = __fsub_rn(u, __fmul_rn(wmin, ds[m].y));
+                        terms[warp][m][lane] = u;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane < MT) {                       // block order: the adds form one dependent chain
+                const int nt = TPB * nblk;
+#pragma unroll
+                for (int i = 0; i < TPB * CHUNK; i++)
+                    if (i < nt) acc = __fadd_rn(acc, terms[warp][lane][i]);
+            }
+            __syncwarp();                          // chunk c's slot and terms are consumed
+        }
+        cp_async_wait<0>();
+        if (lane < MT) out[(long long)lane * N + n] = acc;
+    }
+}
+
+template <int WT>
+cudaError_t launch_m(dim3 g, dim3 b, cudaStream_t s, const uint8_t* w, long long row_bytes, const int8_t* xq,
+                     const float2* xds, float* out, long long M, long long N, long long K) {
+    switch (M) {
+        case 1: mmvq_kernel<WT, 1><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 2: mmvq_kernel<WT, 2><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 3: mmvq_kernel<WT, 3><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 4: mmvq_kernel<WT, 4><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 5: mmvq_kernel<WT, 5><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 6: mmvq_kernel<WT, 6><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 7: mmvq_kernel<WT, 7><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 8: mmvq_kernel<WT, 8><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gemv
+
+cudaError_t run_gemv(int wt, const void* W, long long row_bytes, const void* Xq, float* out, long long M, long long N,
+                     long long K, cudaStream_t s) {
+    if (M < 1 || M > MMVQ_MAX_M || K % 256 != 0) return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long grid = (N + gemv::WARPS - 1) / gemv::WARPS;
+    if (sms > 0 && grid > (long long)sms * 8) grid = (long long)sms * 8;
+    const uint8_t* w = static_cast<const uint8_t*>(W);
+    const int8_t* xq = static_cast<const int8_t*>(Xq);
+    const float2* xds = reinterpret_cast<const float2*>(static_cast<const uint8_t*>(Xq) + M * K);
+    const dim3 g((unsigned)grid), b(gemv::WARPS * 32);
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (wt) {
+        case WT_Q8_0: e = gemv::launch_m<WT_Q8_0>(g, b, s, w, row_bytes, xq, xds, out, M, N, K); break;
+        case WT_Q4_0: e = gemv::launch_m<WT_Q4_0>(g, b, s, w, row_bytes, xq, xds, out, M, N, K); break;
+        case WT_Q4_K: e = gemv::launch_m<WT_Q4_K>(g, b, s, w, row_bytes, xq, xds, out, M, N, K); break;
+        case WT_IQ1_M: e = gemv::launch_m<WT_IQ1_M>(g, b, s, w, row_bytes, xq, xds, out, M, N, K); break;
+        case WT_Q6_K: e = gemv::launch_m<WT_Q6_K>(g, b, s, w, row_bytes, xq, xds, out, M, N, K); break;
+    }
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace mmq

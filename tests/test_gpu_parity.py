@@ -109,6 +109,22 @@ def test_block_gemm_matches_oracle(wtype, shape):
     assert _rel_err(out, ref) <= TOL
 
 
+@pytest.mark.parametrize("wtype", BLOCK_TYPES)
+@pytest.mark.parametrize("shape", [(1, 1, 256), (3, 130, 1280), (8, 257, 4096), (5, 64, 768), (4, 200, 11008)])
+def test_few_token_path_bit_exact(wtype, shape):
+    # M <= 8 (q6_K: 4) runs on the matrix-vector kernel, which forms every block term and sum in the
+    # blockwise definition's order: the f32 output equals the oracle's bit for bit (K = 1280, 768 and
+    # 11008 leave a partial chunk of 32-value blocks)
+    M, N, K = shape
+    if wtype == synth.Q6_K and M > 4:
+        pytest.skip("q6_K takes the matrix-vector kernel up to 4 tokens")
+    pb = synth.make_problem(wtype, M, N, K, seed=13 + M + N + wtype)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm(wtype, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    ref = oracle.gemm(wtype, pb.W, q, d, s, N)
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32)), np.abs(out - ref).max()
+
+
 @pytest.mark.parametrize("wtype", PARTIAL_TYPES)
 @pytest.mark.parametrize("shape", [(3, 5, 256), (131, 200, 512)])
 def test_debug_partials_bit_exact(wtype, shape):
