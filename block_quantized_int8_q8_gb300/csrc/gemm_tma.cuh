@@ -1,28 +1,27 @@
-// gemm_tma.cuh -- the dense production MMQ kernel for the block types: TMA-fed, converter-group
+// gemm_tma.cuh -- the production MMQ kernel of the block types (dense and MoE): TMA-fed, converter-group
 // pipelined, register rescale.
 //
 // Computes out[m,n] = sum_b wd[n,b] * xd[m,b] * I[m,n,b] (Q4_K: minus dmin*m_b*s[m,b]) with the exact
 // per-block integer dot I[m,n,b] = sum_{k in b} xq[m,k] * wq[n,k]  ("A Negative Result on int8
 // Tensor-Core MMQ", §2; "08 · R1 — int8 MMQ prefill GEMM", §2.1-§2.2 and §3.2).
 //
-// Pipeline of one CTA (128 weight rows x 128 tokens, all of K):
+// Pipeline of one CTA (128 weight rows x 128 tokens, all of K or one part of it):
 //   * loader warp (one thread): TMA loads of (a) raw weight bytes, one "super-stage" of 256 k (IQ1_M:
 //     1024 k) for the 128 rows, into a two-slot raw ring; (b) the token operand, fp16 codes of the
 //     q8_1 shadow, 64 k x 128 tokens with the 128-byte swizzle straight into the MMA operand ring;
 //     (c) the tokens' block scales d (Q4_K also s) from the block-major shadow into a scale ring.
-//   * a converter group (two warps, four for IQ1_M): each thread takes two weight rows (one for IQ1_M),
-//     reads its raw bytes from the raw ring (16-byte loads, conflict-free: the row pitch is an odd
-//     number of 16-byte units), unpacks them EXACTLY to fp16 integers (the same unpackers as the
-//     general kernel in gemm.cuh), stores the 128B-swizzled K-major operand row and the row's block
-//     scales.
-//   * MMA warp: two tcgen05.mma kind::f16 (M=128, N=128, K=16) per 32-k block into one of four
-//     128-column TMEM accumulators; a commit per block hands it to the epilogue.
-//   * eight epilogue warps: tcgen05.ld each finished block and apply acc += I * (xd * wd) in packed
+//   * a converter group (two warps; four for IQ1_M and q6_K): each thread takes two weight rows in one
+//     unrolled body (one row for IQ1_M and q6_K), reads its raw bytes from the raw ring (16-byte loads,
+//     conflict-free: the row pitch is an odd number of 16-byte units), unpacks them EXACTLY to fp16
+//     integers (the unpackers of gemm.cuh; q6_K's below), stores the 128B-swizzled K-major operand row
+//     (q6_K: two rows, its sub-block scale split over two exact operands) and the row's block scales.
+//   * MMA warp: four tcgen05.mma kind::f16 (M=128, N=128, K=16) per 64-k stage (q6_K: eight) into one
+//     of two stage buffers of two 128-column TMEM accumulators; a commit per stage hands it on.
+//   * sixteen epilogue warps: tcgen05.ld each finished block and apply acc += I * (xd * wd) in packed
 //     f32 pairs in registers ("A Negative Result", §2-§4: no shared-memory round trip of the
-//     accumulator).  IQ1_M's per-16 scale (2s+1) and Q4_K's 6-bit sub-block scale are folded into the
-//     integer operand (exact), so their block scale is the super-block d (IQ1_M: d/8).
-// Four accumulators decouple the tensor core from the epilogue by four blocks, so the rescale of block
-// b overlaps the MMAs of blocks b+1..b+3.
+//     accumulator).  IQ1_M's per-16 scale (2s+1), Q4_K's 6-bit and q6_K's int8 sub-block scales are
+//     folded into the integer operand (exact), so their block scale is the super-block d (IQ1_M: d/8).
+// Two stage buffers let the MMAs of stage s+1 run while the epilogue rescales stage s.
 #pragma once
 #include <cuda.h>
 #include "gemm.cuh"
@@ -46,9 +45,9 @@ constexpr int EPI_WARPS = 16;         // four per TMEM lane quarter
 constexpr int EPI_COLS = BN * 4 / EPI_WARPS;   // tokens per epilogue thread (32)
 constexpr int EPI_CHUNKS = EPI_COLS / 16;      // 16-column TMEM loads per block
 // Warp roles per weight type: 16 epilogue warps, the converter warps, the MMA warp, the TMA loader warp.
-// Two converter warps (two weight rows per thread) keep up with the rescale for Q8_0 / Q4_0 / Q4_K and
-// leave 96 registers per thread (20 warps); IQ1_M's unpack is the heaviest per row and gets four (22
-// warps, 80 registers).
+// Two converter warps (two weight rows per thread) serve Q8_0 / Q4_0 / Q4_K and leave 96 registers per
+// thread (20 warps; four warps of one row measured slower); the unpacks of IQ1_M and q6_K are the
+// heaviest per row and get four (22 warps, 80 registers; two warps of two rows measured 1.3-1.8x slower).
 template <int WT> struct Warps {
     static constexpr int kConv = (WT == WT_IQ1_M || WT == WT_Q6_K) ? 4 : 2;
     static constexpr int kRowsPerConv = BM / (kConv * 32);
