@@ -30,6 +30,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include "mmq_device.cuh"
+#include "internal.h"
 
 namespace mmq {
 
@@ -778,12 +779,13 @@ template <int WT, int MODE, bool MOE>
 cudaError_t launch_gemm(const GemmParams& p, int grid_y, cudaStream_t stream) {
     using T = KTraits<WT, MODE>;
     using SmemLayout = SmemLayoutT<WT, T::kSB, T::kScaleRing>;
-    static bool configured = false;
+    static bool configured[64] = {};       // per instantiation and device
     auto kern = mmq_gemm_kernel<WT, MODE, MOE>;
-    if (!configured) {
+    bool& done = device_flag(configured);
+    if (!done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::alloc);
         if (e != cudaSuccess) return e;
-        configured = true;
+        done = true;
     }
     dim3 grid((p.N + BM - 1) / BM, grid_y);
     kern<<<grid, NTHREADS, SmemLayout::alloc, stream>>>(p);

@@ -105,15 +105,16 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
     auto kern = tma::mmq_gemm_tma_kernel<WT, false>;
     auto kern_moe = tma::mmq_gemm_tma_kernel<WT, true>;
     auto kern_dbg = tma::mmq_gemm_tma_kernel<WT, false, true>;
-    static bool configured = false;       // per instantiation; the attribute is per function
-    if (!configured) {
+    static bool configured[64] = {};      // per instantiation and device; the attribute is per function
+    bool& done = device_flag(configured);
+    if (!done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern_moe, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern_dbg, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e != cudaSuccess) return e;
-        configured = true;
+        done = true;
     }
     const long long ntn = (a.N + BM - 1) / BM;
     if (dbg) {                              // block sums: one CTA per tile, whole K range
@@ -179,12 +180,13 @@ cudaError_t run_gemm_w8a8_tma(const void* W, const void* X, void* out, long long
     const float* ws = reinterpret_cast<const float*>(static_cast<const uint8_t*>(W) + N * K);
     const float* xs = reinterpret_cast<const float*>(static_cast<const uint8_t*>(X) + M * K);
     auto kern = w8tma::mmq_w8a8_tma_kernel;
-    static bool configured = false;
-    if (!configured) {
+    static bool configured[64] = {};
+    bool& done = device_flag(configured);
+    if (!done) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, w8tma::Smem::alloc);
         if (e != cudaSuccess) return e;
-        configured = true;
+        done = true;
     }
     const long long tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
     kern<<<(unsigned)tiles, w8tma::NTHREADS, w8tma::Smem::alloc, stream>>>(

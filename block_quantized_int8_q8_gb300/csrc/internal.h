@@ -103,6 +103,16 @@ bool route_fused_supported(long long M, int slots, int E);
 cudaError_t run_route_fused(const int32_t* ids, int M, int slots, int E, int tile_n, const RouteWorkspace& ws,
                             cudaStream_t s);
 
+// Per-device once-flags for function attributes (cudaFuncSetAttribute acts on the current device's
+// context): the current device's flag in `flags`, or a scratch flag (always false) past 64 devices.
+inline bool& device_flag(bool (&flags)[64]) {
+    static thread_local bool scratch;
+    int dev = 0;
+    scratch = false;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return scratch;
+    return flags[dev];
+}
+
 // Per-translation-unit device error words: read, OR into *bits, clear.
 cudaError_t read_clear_errors_quantize(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_route(unsigned* bits, cudaStream_t s);
