@@ -126,6 +126,7 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
     if (a.work != nullptr) {                // MoE: one CTA per (work item, weight-row tile) + tail parts
         const tma::MoeTiles moe{a.work, a.nwork, a.gstart, a.rowlist, sm_count(), moe_kparts(WT, a.K)};
         const long long ctas = ntn * a.max_work + moe.sms;
+        if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;   // beyond the grid's x extent
         kern_moe<<<(unsigned)ctas, tma::Warps<WT>::kThreads, L::alloc, stream>>>(
             tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)ctas, 0, moe);
         return cudaGetLastError();

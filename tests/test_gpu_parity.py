@@ -125,6 +125,18 @@ def test_few_token_path_bit_exact(wtype, shape):
     assert np.array_equal(out.view(np.uint32), ref.view(np.uint32)), np.abs(out - ref).max()
 
 
+@pytest.mark.parametrize("wtype", [synth.Q6_K, synth.Q4_K])
+def test_small_grid_k_parts_at_super_stage_boundaries(wtype):
+    # 2 tiles on a 152-SM part: every tile runs in 16 K parts; K = 11008 has 43 super-stages, so the
+    # parts hold 2 or 3 of them
+    M, N, K = 40, 200, 11008
+    pb = synth.make_problem(wtype, M, N, K, seed=73 + wtype)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm(wtype, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    assert api.read_device_errors() == 0
+    assert _rel_err(out, oracle.gemm(wtype, pb.W, q, d, s, N)) <= TOL
+
+
 @pytest.mark.parametrize("wtype", PARTIAL_TYPES)
 @pytest.mark.parametrize("shape", [(3, 5, 256), (131, 200, 512)])
 def test_debug_partials_bit_exact(wtype, shape):
@@ -268,6 +280,21 @@ def test_gemm_id_tma_tail_split(E):
     for t in range(0, M, 7):
         for j in range(slots):
             assert _rel_err(out[t, j], ref[t, j]) <= TOL, (t, j)
+
+
+def test_gemm_id_tma_path_with_three_kernel_routing():
+    # 8200 tokens x 8 slots = 65 600 routed rows: past the single-block routing kernel's limit, so the
+    # three-kernel route feeds the gather and the TMA-fed grouped GEMM
+    M, E, slots, N, K = 8200, 96, 8, 130, 256
+    pb = synth.make_problem(synth.Q4_0, M, N, K, seed=69, experts=E, slots=slots)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm_id(synth.Q4_0, _dev(pb.W.reshape(-1)), E, xq, _dev(pb.ids), M, N, K).cpu().numpy()
+    assert api.read_device_errors() == 0
+    rows = np.arange(0, M, 97)
+    ref = oracle.gemm_id(synth.Q4_0, pb.W, E, q[rows], d[rows], s[rows], pb.ids[rows], N)
+    for i, t in enumerate(rows):
+        for j in range(slots):
+            assert _rel_err(out[t, j], ref[i, j]) <= TOL, (t, j)
 
 
 def test_gemm_id_tma_path_skewed_routing():
