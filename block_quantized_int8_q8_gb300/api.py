@@ -20,7 +20,7 @@ DEVERR_TIMEOUT, DEVERR_EXPERT_ID, DEVERR_DUP_EXPERT = 1, 2, 4
 #: every symbol include/mmq.h declares
 EXPORTS = ("mmq_status_string", "mmq_last_cuda_error", "mmq_q8_1_bytes", "mmq_weight_bytes", "mmq_w8a8_act_bytes", "mmq_quantize_q8_1",
            "mmq_gemm", "mmq_gemm_id_workspace_bytes", "mmq_gemm_id", "mmq_gemm_debug_partials",
-           "mmq_gemm_debug_block_sums",
+           "mmq_gemm_debug_block_sums", "mmq_selftest_bounded_wait",
            "mmq_read_device_errors", "mmq_gemm_id_noalloc", "mmq_q8_1_prepare")
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -69,6 +69,8 @@ def load():
     lib.mmq_gemm_debug_partials.restype = I
     lib.mmq_gemm_debug_block_sums.argtypes = [I, P, P, P, I64, I64, I64, P]
     lib.mmq_gemm_debug_block_sums.restype = I
+    lib.mmq_selftest_bounded_wait.argtypes = [P, P]
+    lib.mmq_selftest_bounded_wait.restype = I
     lib.mmq_gemm_id_noalloc.argtypes = [I, P, I, P, P, I, P, I64, I64, I64, P]
     lib.mmq_gemm_id_noalloc.restype = I
     lib.mmq_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), P]
@@ -232,3 +234,10 @@ def read_device_errors(stream=None) -> int:
     bits = ctypes.c_uint(0)
     _check(load().mmq_read_device_errors(ctypes.byref(bits), _stream(stream)), "mmq_read_device_errors")
     return bits.value
+
+
+def selftest_bounded_wait(device="cuda", stream=None) -> list[int]:
+    """mmq_selftest_bounded_wait: [completed, abort_flag] of the polling and of the sleeping wait."""
+    res = torch.full((4,), -1, dtype=torch.int32, device=device)
+    _check(load().mmq_selftest_bounded_wait(_ptr(res), _stream(stream)), "mmq_selftest_bounded_wait")
+    return res.cpu().tolist()

@@ -350,6 +350,13 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
     return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm_id");
 }
 
+mmq_status mmq_selftest_bounded_wait(int32_t* result, mmq_stream_t stream) {
+    if (!result) return MMQ_ERR_INVALID_ARG;
+    if (!aligned16(result)) return MMQ_ERR_ALIGN;
+    const cudaError_t e = run_wait_timeout_selftest(result, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_selftest_bounded_wait");
+}
+
 mmq_status mmq_read_device_errors(unsigned* bits, mmq_stream_t stream) {
     if (!bits) return MMQ_ERR_INVALID_ARG;
     *bits = 0;
@@ -358,7 +365,8 @@ mmq_status mmq_read_device_errors(unsigned* bits, mmq_stream_t stream) {
     cudaError_t (*readers[])(unsigned*, cudaStream_t) = {read_clear_errors_quantize, read_clear_errors_route,
                                                          read_clear_errors_q8_0,     read_clear_errors_q4_0,
                                                          read_clear_errors_q4_k,     read_clear_errors_iq1_m,
-                                                         read_clear_errors_w8a8,     read_clear_errors_tma};
+                                                         read_clear_errors_w8a8,     read_clear_errors_tma,
+                                                         read_clear_errors_selftest};
     for (auto r : readers) {
         cudaError_t ei = r(bits, s);
         if (ei != cudaSuccess) e = ei;

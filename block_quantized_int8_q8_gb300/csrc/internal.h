@@ -122,6 +122,9 @@ cudaError_t read_clear_errors_q4_k(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_iq1_m(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_w8a8(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_tma(unsigned* bits, cudaStream_t s);
+cudaError_t read_clear_errors_selftest(unsigned* bits, cudaStream_t s);
+// Device self-test of the bounded waits (selftest.cu): result int32 [4].
+cudaError_t run_wait_timeout_selftest(int* result, cudaStream_t s);
 }  // namespace mmq
 
 // Defines read_clear_errors_<name> for the translation unit that expands it.

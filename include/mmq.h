@@ -214,6 +214,16 @@ mmq_status mmq_gemm_debug_partials(mmq_type wtype, const void* W, const void* Xq
  */
 mmq_status mmq_read_device_errors(unsigned* bits, mmq_stream_t stream);
 
+/*
+ * mmq_selftest_bounded_wait -- device self-test of the bounded pipeline waits.  Two CTAs each wait on a
+ * shared-memory mbarrier that nothing arrives at, one with the polling wait and one with the sleeping
+ * wait the pipelines use.  Each wait must give up after the library's time limit (~2 s), raise its CTA's
+ * abort flag, record MMQ_DEVERR_TIMEOUT and return; the kernel then exits normally.
+ * result : int32 [4], device, 16-byte aligned: per CTA {wait completed (0 expected), abort flag (1)}.
+ * Enqueues on `stream`; read the error bits with mmq_read_device_errors afterwards.
+ */
+mmq_status mmq_selftest_bounded_wait(int32_t* result, mmq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -345,6 +345,21 @@ def test_gemm_id_out_of_range_ids_flagged_and_skipped():
                 assert _rel_err(o[t, j], ref[t, j]) <= TOL
 
 
+# ---------------------------------------------------------------------------------------- failure handling
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable():
+    # a barrier that nothing arrives at: both wait flavours give up, flag the CTA and record the timeout
+    res = api.selftest_bounded_wait(DEV)
+    assert res == [0, 1, 0, 1], res
+    assert api.read_device_errors() & api.DEVERR_TIMEOUT
+    assert api.read_device_errors() == 0                   # read and cleared
+    # the context still runs the product
+    M, N, K = 64, 130, 512
+    pb = synth.make_problem(synth.Q4_0, M, N, K, seed=81)
+    q, d, s, xq = _oracle_acts(pb)
+    out = api.gemm(synth.Q4_0, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    assert _rel_err(out, oracle.gemm(synth.Q4_0, pb.W, q, d, s, N)) <= TOL
+
+
 # ---------------------------------------------------------------------------------------- degenerate sizes
 def test_empty_inputs_are_noops():
     W = torch.zeros(1024, dtype=torch.uint8, device=DEV)
