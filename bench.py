@@ -500,7 +500,7 @@ def main():
             "rescale_ceiling": rescale_ceiling(wt, ops, ffma),
             "e2e": e2e, "gpu_launches": launches_per_step * K_steps, "clocks": clocks,
             "wall_s": wall, "device_errors": errs}
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the oracle baseline is a one-GPU figure
         line["cpu_baseline"] = cpu_baseline(pb, name, args.cpu_baseline_s)
     if rank == 0:
         print(json.dumps(line), flush=True)
