@@ -30,71 +30,94 @@ __host__ __device__ constexpr int chunk_bytes(int wt) {
 }
 __host__ __device__ constexpr bool per16(int wt) { return wt == WT_IQ1_M || wt == WT_Q6_K; }
 
-// 32-bit word at byte offset o of the staged chunk (any alignment).
-__device__ __forceinline__ uint32_t st_word(const uint32_t* st, int o) {
-    return __funnelshift_r(st[o >> 2], st[(o >> 2) + 1], 8 * (o & 3));
+// NW consecutive 32-bit words starting at byte offset o of the staged bytes (any alignment): NW + 1
+// aligned loads and a funnel shift each.
+template <int NW>
+__device__ __forceinline__ void st_span(const uint32_t* st, int o, uint32_t (&w)[NW]) {
+    const uint32_t* p = st + (o >> 2);
+    const int sh = 8 * (o & 3);
+    uint32_t prev = p[0];
+#pragma unroll
+    for (int k = 0; k < NW; k++) {
+        const uint32_t nxt = p[k + 1];
+        w[k] = __funnelshift_r(prev, nxt, sh);
+        prev = nxt;
+    }
 }
-__device__ __forceinline__ float st_half(const uint32_t* st, int o) {
-    return __half2float(__ushort_as_half((unsigned short)(st_word(st, o) & 0xFFFFu)));
-}
-// Field [pos, pos + width) of a little-endian bit stream starting at byte o (width <= 8).
-__device__ __forceinline__ uint32_t st_field(const uint32_t* st, int o, int pos, int width) {
-    return (st_word(st, o + (pos >> 3)) >> (pos & 7)) & ((1u << width) - 1u);
-}
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
 
-// Decode block j (0..31) of the staged chunk: 8 words of int8 values in k order and the scale factors of
-// the blockwise definition (per 32 values, or per 16-value half: wsc[0], wsc[1]).
+// Decode block j of the staged bytes st: 8 words of int8 values in k order and the scale factors of the
+// blockwise definition (per 32 values, or per 16-value half: wsc[0], wsc[1]).  Super-block types start
+// every record on a 4-byte boundary and read aligned words; Q8_0 and Q4_0 blocks are 2-byte aligned.
 template <int WT>
 __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t (&w)[8], float (&wsc)[2],
                                              float& wmin) {
     wmin = 0.f;
     if constexpr (WT == WT_Q8_0) {                 // f16 d | int8 q[32]
-        const int o = 34 * j;
-        wsc[0] = wsc[1] = st_half(st, o);
+        uint32_t b[9];                             // bytes 34j .. 34j + 35
+        st_span<9>(st, 34 * j, b);
+        wsc[0] = wsc[1] = half_lo(b[0]);
 #pragma unroll
-        for (int k = 0; k < 8; k++) w[k] = st_word(st, o + 2 + 4 * k);
+        for (int k = 0; k < 8; k++) w[k] = __funnelshift_r(b[k], b[k + 1], 16);
     } else if constexpr (WT == WT_Q4_0) {          // f16 d | byte i = code i (low) | code i+16 (high)
-        const int o = 18 * j;
-        wsc[0] = wsc[1] = st_half(st, o);
+        uint32_t b[5];                             // bytes 18j .. 18j + 19
+        st_span<5>(st, 18 * j, b);
+        wsc[0] = wsc[1] = half_lo(b[0]);
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            const uint32_t nw = st_word(st, o + 2 + 4 * k);
+            const uint32_t nw = __funnelshift_r(b[k], b[k + 1], 16);
             w[k] = __vsub4(nw & 0x0F0F0F0Fu, 0x08080808u);            // code - 8
             w[4 + k] = __vsub4((nw >> 4) & 0x0F0F0F0Fu, 0x08080808u);
         }
     } else if constexpr (WT == WT_Q4_K) {          // f16 d | f16 dmin | 12 B six-bit sc, m | 128 B codes
-        const int o = 144 * (j >> 3), sb = j & 7;
-        const float d = st_half(st, o), dmin = st_half(st, o + 2);
-        wsc[0] = wsc[1] = __fmul_rn(d, (float)st_field(st, o + 4, 6 * sb, 6));
-        wmin = __fmul_rn(dmin, (float)st_field(st, o + 4, 6 * (8 + sb), 6));
-        const int co = o + 16 + 32 * (sb >> 1), sh = 4 * (sb & 1);  // sub-block 2p (low) / 2p+1 (high nibbles)
+        const uint32_t* rec = st + 36 * (j >> 3);  // 144-byte records
+        const int sb = j & 7;
+        const uint32_t h0 = rec[0];
+        const uint64_t f = (uint64_t)rec[1] | ((uint64_t)rec[2] << 32);  // fields 0..10 (bits 0..63)
+        const uint32_t f2 = rec[3];                                      // bits 64..95
+        auto field = [&](int pos) -> uint32_t {
+            return pos + 6 <= 64 ? (uint32_t)(f >> pos) & 63u
+                                 : (pos >= 64 ? (f2 >> (pos - 64)) & 63u
+                                              : (uint32_t)((f >> pos) | ((uint64_t)f2 << (64 - pos))) & 63u);
+        };
+        wsc[0] = wsc[1] = __fmul_rn(half_lo(h0), (float)field(6 * sb));
+        wmin = __fmul_rn(half_hi(h0), (float)field(6 * (8 + sb)));
+        const uint32_t* codes = rec + 4 + 8 * (sb >> 1);                 // sub-block 2p (low) / 2p+1 (high)
+        const int sh = 4 * (sb & 1);
 #pragma unroll
-        for (int k = 0; k < 8; k++) w[k] = (st_word(st, co + 4 * k) >> sh) & 0x0F0F0F0Fu;
+        for (int k = 0; k < 8; k++) w[k] = (codes[k] >> sh) & 0x0F0F0F0Fu;
     } else if constexpr (WT == WT_IQ1_M) {         // 64 B codes | 4 B signs | 6 B three-bit s | f16 d
-        const int o = 76 * (j >> 3), sb = j & 7;
-        const float d = st_half(st, o + 74);
+        const uint32_t* rec = st + 19 * (j >> 3);  // 76-byte records
+        const int sb = j & 7;
+        const uint64_t sbits = (uint64_t)rec[17] | ((uint64_t)rec[18] << 32);   // bytes 68..75
+        const float d = half_hi(rec[18]);                                         // bytes 74..75
 #pragma unroll
         for (int h = 0; h < 2; h++)
-            wsc[h] = __fmul_rn(__fmul_rn(d, (float)(2u * st_field(st, o + 68, 3 * (2 * sb + h), 3) + 1u)), 0.125f);
-        const uint32_t signs = st_word(st, o + 64) >> (4 * sb);        // one bit per 8 values
+            wsc[h] = __fmul_rn(__fmul_rn(d, (float)(2u * (uint32_t)((sbits >> (3 * (2 * sb + h))) & 7u) + 1u)), 0.125f);
+        const uint32_t signs = rec[16] >> (4 * sb);                      // one bit per 8 values
+        const uint32_t cw[2] = {rec[2 * sb], rec[2 * sb + 1]};           // codes of the block's 32 values
 #pragma unroll
         for (int k = 0; k < 8; k++) {
-            const uint32_t cb = st_word(st, o + 8 * sb + k) & 0xFFu;    // codes of values 4k..4k+3
+            const uint32_t cb = (cw[k >> 2] >> (8 * (k & 3))) & 0xFFu;    // codes of values 4k..4k+3
             const uint32_t c = (cb & 3u) | ((cb & 0x0Cu) << 6) | ((cb & 0x30u) << 12) | ((cb & 0xC0u) << 18);
             // 8 * (code - 1) + (+1 | -1), per byte: 8 * code + (-7 | -9)
             w[k] = __vadd4(c << 3, ((signs >> (k >> 1)) & 1u) ? 0xF7F7F7F7u : 0xF9F9F9F9u);
         }
     } else {                                        // q6_K: int8 sc[16] | f16 d | pad | four 48 B records
-        const int o = 224 * (j >> 3), sb = j & 7;
-        const float d = st_half(st, o + 16);
+        const uint32_t* rec = st + 56 * (j >> 3);  // 224-byte records
+        const int sb = j & 7;
+        const float d = half_lo(rec[4]);
+        const uint32_t scw = rec[sb >> 1] >> (16 * (sb & 1));            // sc of sub-blocks 2sb, 2sb + 1
 #pragma unroll
-        for (int h = 0; h < 2; h++) wsc[h] = __fmul_rn(d, (float)(int8_t)(st_word(st, o + 2 * sb + h) & 0xFFu));
-        const int rec = o + 32 + 48 * (sb >> 1), hh = sb & 1;           // record of the 64-value stage
+        for (int h = 0; h < 2; h++) wsc[h] = __fmul_rn(d, (float)(int8_t)((scw >> (8 * h)) & 0xFFu));
+        const uint32_t* lo = rec + 8 + 12 * (sb >> 1);                   // stage record: 8 low, 4 high words
+        const int hh = sb & 1;
 #pragma unroll
-        for (int k = 0; k < 8; k++) {                                   // values 32hh + 4k .. + 3 of the stage
-            const uint32_t lo = (st_word(st, rec + 4 * k) >> (4 * hh)) & 0x0F0F0F0Fu;
-            const uint32_t hi = ((st_word(st, rec + 32 + 4 * (k & 3)) >> (2 * (2 * hh + (k >> 2)))) & 0x03030303u) << 4;
-            w[k] = __vsub4(lo | hi, 0x20202020u);                       // code - 32
+        for (int k = 0; k < 8; k++) {                                    // values 32hh + 4k .. + 3 of the stage
+            const uint32_t l = (lo[k] >> (4 * hh)) & 0x0F0F0F0Fu;
+            const uint32_t hi = ((lo[8 + (k & 3)] >> (2 * (2 * hh + (k >> 2)))) & 0x03030303u) << 4;
+            w[k] = __vsub4(l | hi, 0x20202020u);                         // code - 32
         }
     }
 }
@@ -111,7 +134,8 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
                                                         int N, int K) {
     constexpr int TPB = per16(WT) ? 2 : 1;        // terms per block
     __shared__ __align__(16) uint32_t stage[WARPS][DEPTH][STAGE_WORDS_16];
-    __shared__ float terms[WARPS][MT][TPB * CHUNK + 1];   // odd row pitch: the summing lanes' reads hit distinct banks
+    // row pitch 4 mod 32 words: the summing lanes' 16-byte reads fall in distinct banks
+    __shared__ __align__(16) float terms[WARPS][MT][TPB * CHUNK + 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = K / 32, nchunks = (nb + CHUNK - 1) / CHUNK;
     const bool row16 = (row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(W) & 15) == 0;
@@ -181,9 +205,17 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
             __syncwarp();
             if (lane < MT) {                       // block order: the adds form one dependent chain
                 const int nt = TPB * nblk;
+                const float4* tp = reinterpret_cast<const float4*>(terms[warp][lane]);
 #pragma unroll
-                for (int i = 0; i < TPB * CHUNK; i++)
-                    if (i < nt) acc = __fadd_rn(acc, terms[warp][lane][i]);
+                for (int q = 0; q < TPB * CHUNK / 4; q++) {
+                    if (4 * q < nt) {              // nt is a multiple of 8: K % 256 == 0
+                        const float4 v = tp[q];
+                        acc = __fadd_rn(acc, v.x);
+                        acc = __fadd_rn(acc, v.y);
+                        acc = __fadd_rn(acc, v.z);
+                        acc = __fadd_rn(acc, v.w);
+                    }
+                }
             }
             __syncwarp();                          // chunk c's slot and terms are consumed
         }

@@ -111,11 +111,12 @@ def test_block_gemm_matches_oracle(wtype, shape):
 
 
 @pytest.mark.parametrize("wtype", BLOCK_TYPES)
-@pytest.mark.parametrize("shape", [(1, 1, 256), (3, 130, 1280), (8, 257, 4096), (5, 64, 768), (4, 200, 11008)])
+@pytest.mark.parametrize("shape", [(1, 1, 256), (3, 130, 1280), (8, 257, 4096), (5, 64, 768), (4, 200, 11008),
+                                   (2, 40001, 256), (7, 3, 512)])
 def test_few_token_path_bit_exact(wtype, shape):
     # M <= 8 (q6_K: 4) runs on the matrix-vector kernel, which forms every block term and sum in the
     # blockwise definition's order: the f32 output equals the oracle's bit for bit (K = 1280, 768 and
-    # 11008 leave a partial chunk of 32-value blocks)
+    # 11008 leave a partial chunk of 32-value blocks; 40001 rows outnumber one pass of the grid)
     M, N, K = shape
     if wtype == synth.Q6_K and M > 4:
         pytest.skip("q6_K takes the matrix-vector kernel up to 4 tokens")
