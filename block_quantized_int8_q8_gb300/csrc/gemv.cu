@@ -19,16 +19,19 @@
 namespace mmq {
 namespace gemv {
 
-constexpr int WARPS = 8;                 // rows in flight per CTA
+constexpr int WARPS = 4;                 // rows in flight per CTA (small CTAs balance the rows over the SMs)
 constexpr int CHUNK = 32;                // 32-value blocks per chunk (one per lane)
-constexpr int STAGE_WORDS = 1088 / 4 + 1;   // largest chunk (Q8_0: 32 x 34 B) plus one word of overrun
-constexpr int STAGE_WORDS_16 = (STAGE_WORDS + 3) / 4 * 4;   // ring slots on 16-byte boundaries
 
 // Raw bytes of one chunk (32 blocks = 1024 values) per type.
 __host__ __device__ constexpr int chunk_bytes(int wt) {
     return wt == WT_Q8_0 ? 32 * 34 : wt == WT_Q4_0 ? 32 * 18 : wt == WT_Q4_K ? 4 * 144 : wt == WT_IQ1_M ? 4 * 76 : 4 * 224;
 }
 __host__ __device__ constexpr bool per16(int wt) { return wt == WT_IQ1_M || wt == WT_Q6_K; }
+// A ring slot: one chunk plus one word that the last block's span read may touch, on 16-byte boundaries.
+__host__ __device__ constexpr int stage_words(int wt) { return (chunk_bytes(wt) / 4 + 1 + 3) / 4 * 4; }
+// Ring slots per warp: DEPTH - 1 chunks in flight while one is decoded.  IQ1_M's chunks are the smallest
+// (304 B) and it gains from five slots at 4-8 tokens; the others measured best at three.
+__host__ __device__ constexpr int depth(int wt) { return wt == WT_IQ1_M ? 5 : 3; }
 
 // NW consecutive 32-bit words starting at byte offset o of the staged bytes (any alignment): NW + 1
 // aligned loads and a funnel shift each.
@@ -46,6 +49,10 @@ __device__ __forceinline__ void st_span(const uint32_t* st, int o, uint32_t (&w)
 }
 __device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
 __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+// bias_byte: for unsigned bytes u with u + (128 - c) < 256 (so no carry leaves the byte), the int8 value
+// u - c is ((u + (128 - c)) ^ 0x80) per byte: one add and one xor for four bytes at once.  Used with c = 8
+// (4-bit codes), 32 (6-bit codes) and 9 or 7 (IQ1_M's 8 * code in {0, 8, 16, 24}).
 
 // Decode block j of the staged bytes st: 8 words of int8 values in k order and the scale factors of the
 // blockwise definition (per 32 values, or per 16-value half: wsc[0], wsc[1]).  Super-block types start
@@ -67,8 +74,8 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const uint32_t nw = __funnelshift_r(b[k], b[k + 1], 16);
-            w[k] = __vsub4(nw & 0x0F0F0F0Fu, 0x08080808u);            // code - 8
-            w[4 + k] = __vsub4((nw >> 4) & 0x0F0F0F0Fu, 0x08080808u);
+            w[k] = ((nw & 0x0F0F0F0Fu) + 0x78787878u) ^ 0x80808080u;         // code - 8 (see bias_byte)
+            w[4 + k] = (((nw >> 4) & 0x0F0F0F0Fu) + 0x78787878u) ^ 0x80808080u;
         }
     } else if constexpr (WT == WT_Q4_K) {          // f16 d | f16 dmin | 12 B six-bit sc, m | 128 B codes
         const uint32_t* rec = st + 36 * (j >> 3);  // 144-byte records
@@ -101,8 +108,8 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
         for (int k = 0; k < 8; k++) {
             const uint32_t cb = (cw[k >> 2] >> (8 * (k & 3))) & 0xFFu;    // codes of values 4k..4k+3
             const uint32_t c = (cb & 3u) | ((cb & 0x0Cu) << 6) | ((cb & 0x30u) << 12) | ((cb & 0xC0u) << 18);
-            // 8 * (code - 1) + (+1 | -1), per byte: 8 * code + (-7 | -9)
-            w[k] = __vadd4(c << 3, ((signs >> (k >> 1)) & 1u) ? 0xF7F7F7F7u : 0xF9F9F9F9u);
+            // 8 * (code - 1) + (+1 | -1), per byte: 8 * code + (-7 | -9) (see bias_byte)
+            w[k] = ((c << 3) + (((signs >> (k >> 1)) & 1u) ? 0x77777777u : 0x79797979u)) ^ 0x80808080u;
         }
     } else {                                        // q6_K: int8 sc[16] | f16 d | pad | four 48 B records
         const uint32_t* rec = st + 56 * (j >> 3);  // 224-byte records
@@ -117,7 +124,7 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
         for (int k = 0; k < 8; k++) {                                    // values 32hh + 4k .. + 3 of the stage
             const uint32_t l = (lo[k] >> (4 * hh)) & 0x0F0F0F0Fu;
             const uint32_t hi = ((lo[8 + (k & 3)] >> (2 * (2 * hh + (k >> 2)))) & 0x03030303u) << 4;
-            w[k] = __vsub4(l | hi, 0x20202020u);                         // code - 32
+            w[k] = ((l | hi) + 0x60606060u) ^ 0x80808080u;                // code - 32 (see bias_byte)
         }
     }
 }
@@ -125,7 +132,6 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
 // Grid-stride over weight rows, one row per warp at a time; MT tokens.  xq: int8 codes [MT][K];
 // xds: (d, s) [MT][K/32].  The row's chunks stream into a DEPTH-slot shared-memory ring with cp.async, so
 // DEPTH - 1 chunks of the weight stream are in flight while one is decoded.
-constexpr int DEPTH = 3;
 
 template <int WT, int MT>
 __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restrict__ W, long long row_bytes,
@@ -133,7 +139,8 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
                                                         const float2* __restrict__ xds, float* __restrict__ out,
                                                         int N, int K) {
     constexpr int TPB = per16(WT) ? 2 : 1;        // terms per block
-    __shared__ __align__(16) uint32_t stage[WARPS][DEPTH][STAGE_WORDS_16];
+    constexpr int DEPTH = depth(WT);
+    __shared__ __align__(16) uint32_t stage[WARPS][DEPTH][stage_words(WT)];
     // row pitch 4 mod 32 words: the summing lanes' 16-byte reads fall in distinct banks
     __shared__ __align__(16) float terms[WARPS][MT][TPB * CHUNK + 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,7 +257,7 @@ cudaError_t run_gemv(int wt, const void* W, long long row_bytes, const void* Xq,
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     long long grid = (N + gemv::WARPS - 1) / gemv::WARPS;
-    if (sms > 0 && grid > (long long)sms * 8) grid = (long long)sms * 8;
+    if (sms > 0 && grid > (long long)sms * (64 / gemv::WARPS)) grid = (long long)sms * (64 / gemv::WARPS);
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const int8_t* xq = static_cast<const int8_t*>(Xq);
     const float2* xds = reinterpret_cast<const float2*>(static_cast<const uint8_t*>(Xq) + M * K);
