@@ -3,7 +3,7 @@
 // small batches run on the matrix-vector path; the MMQ tiles win from ~100 tokens on).
 //
 // One warp per weight row.  The row is walked in chunks of 32 blocks of 32 values, one block per lane:
-// the warp stages the chunk's raw bytes in shared memory with coalesced 4-byte loads, each lane decodes
+// the warp stages the chunk's raw bytes in shared memory with coalesced cp.async copies, each lane decodes
 // its block to int8 words, forms the exact int32 block dot per token with dp4a ("08 · R1 — int8 MMQ
 // prefill GEMM", §2.1: the in-block integer dot is exact), and its f32 term u = (xd * wsc) * I
 // (Q4_K: minus dmin*m_b * s; IQ1_M and q6_K: one term per 16-value half).  Lane m then adds the chunk's
@@ -132,7 +132,6 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
 // Grid-stride over weight rows, one row per warp at a time; MT tokens.  xq: int8 codes [MT][K];
 // xds: (d, s) [MT][K/32].  The row's chunks stream into a DEPTH-slot shared-memory ring with cp.async, so
 // DEPTH - 1 chunks of the weight stream are in flight while one is decoded.
-
 template <int WT, int MT>
 __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restrict__ W, long long row_bytes,
                                                         const int8_t* __restrict__ xq,
