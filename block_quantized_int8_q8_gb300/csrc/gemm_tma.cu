@@ -105,6 +105,10 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
     auto kern = tma::mmq_gemm_tma_kernel<WT, false>;
     auto kern_moe = tma::mmq_gemm_tma_kernel<WT, true>;
     auto kern_dbg = tma::mmq_gemm_tma_kernel<WT, false, true>;
+    // at most 64 tokens: four converter warps (the same kernel for the types that always use four)
+    constexpr int kSmallConv = 4;
+    constexpr long long kSmallM = 64;
+    auto kern_small = tma::mmq_gemm_tma_kernel<WT, false, false, kSmallConv>;
     static bool configured[64] = {};      // per instantiation and device; the attribute is per function
     bool& done = device_flag(configured);
     if (!done) {
@@ -113,6 +117,8 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
             e = cudaFuncSetAttribute(kern_moe, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern_dbg, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern_small, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
         if (e != cudaSuccess) return e;
         done = true;
     }
@@ -159,8 +165,12 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
         if (e != cudaSuccess) return e;
     }
     const dim3 grid((unsigned)(nfull + (split_rows * ntn << lgp)));
-    kern<<<grid, tma::Warps<WT>::kThreads, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K,
-                                                    (int)ntn, (int)nfull, lgp, tma::MoeTiles{});
+    if (a.M <= kSmallM)
+        kern_small<<<grid, tma::Warps<WT, kSmallConv>::kThreads, L::alloc, stream>>>(
+            tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N, (int)a.K, (int)ntn, (int)nfull, lgp, tma::MoeTiles{});
+    else
+        kern<<<grid, tma::Warps<WT>::kThreads, L::alloc, stream>>>(tm_raw, tm_b, tm_xd, tm_xs, a.out, (int)a.M, (int)a.N,
+                                                        (int)a.K, (int)ntn, (int)nfull, lgp, tma::MoeTiles{});
     return cudaGetLastError();
 }
 

@@ -46,10 +46,13 @@ constexpr int EPI_COLS = BN * 4 / EPI_WARPS;   // tokens per epilogue thread (32
 constexpr int EPI_CHUNKS = EPI_COLS / 16;      // 16-column TMEM loads per block
 // Warp roles per weight type: 16 epilogue warps, the converter warps, the MMA warp, the TMA loader warp.
 // Two converter warps (two weight rows per thread) serve Q8_0 / Q4_0 / Q4_K and leave 96 registers per
-// thread (20 warps; four warps of one row measured slower); the unpacks of IQ1_M and q6_K are the
-// heaviest per row and get four (22 warps, 80 registers; two warps of two rows measured 1.3-1.8x slower).
-template <int WT> struct Warps {
-    static constexpr int kConv = (WT == WT_IQ1_M || WT == WT_Q6_K) ? 4 : 2;
+// thread (20 warps; four warps of one row measured slower from 128 tokens on); the unpacks of IQ1_M and
+// q6_K are the heaviest per row and get four (22 warps, 80 registers; two warps of two rows measured
+// 1.3-1.8x slower).  CV overrides the converter count: dense grids of at most 64 tokens, whose epilogue
+// warps are mostly idle, run Q8_0 / Q4_0 / Q4_K with four (Q4_K 16-64 tokens: 12-20 % faster).
+template <int WT> constexpr int default_conv() { return (WT == WT_IQ1_M || WT == WT_Q6_K) ? 4 : 2; }
+template <int WT, int CV = default_conv<WT>()> struct Warps {
+    static constexpr int kConv = CV;
     static constexpr int kRowsPerConv = BM / (kConv * 32);
     static constexpr int kConv0 = EPI_WARPS;
     static constexpr int kMma = kConv0 + kConv;
@@ -215,8 +218,8 @@ template <int WT> struct Bars {
     }
 };
 
-// Convert operand stage s = t*SS + J of raw super-stage t (this thread: weight rows c.pt + 64*i).
-template <int WT, int J>
+// Convert operand stage s = t*SS + J of raw super-stage t (this thread: weight rows c.pt + 32*CV*i).
+template <int WT, int CV, int J>
 __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t raw) {
     using L = Smem<WT>;
     using B = Bars<WT>;
@@ -233,8 +236,8 @@ __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t raw) {
     // both rows of a 2-row thread in one unrolled body: the second row's raw loads and unpack overlap the
     // first's (measured +9 % on Q4_0, +4 % on Q4_K against one row at a time)
 #pragma unroll
-    for (int rr = 0; rr < Warps<WT>::kRowsPerConv; rr++) {
-        const int row = c.pt + rr * Warps<WT>::kConv * 32;
+    for (int rr = 0; rr < Warps<WT, CV>::kRowsPerConv; rr++) {
+        const int row = c.pt + rr * CV * 32;
         RawA r;
         load_raw<WT, J>(raw + row * Geom<WT>::U * 16, r);
         float wsc[2], wmn[2] = {0.f, 0.f};
@@ -267,19 +270,19 @@ __device__ __forceinline__ void convert_stage(Ctx& c, int t, uint32_t raw) {
     }
 }
 
-template <int WT, int J, int NJ>
+template <int WT, int CV, int J, int NJ>
 struct ConvUnroll {
     __device__ static __forceinline__ void run(Ctx& c, int t, uint32_t rrow) {
-        convert_stage<WT, J>(c, t, rrow);
-        ConvUnroll<WT, J + 1, NJ>::run(c, t, rrow);
+        convert_stage<WT, CV, J>(c, t, rrow);
+        ConvUnroll<WT, CV, J + 1, NJ>::run(c, t, rrow);
     }
 };
-template <int WT, int NJ>
-struct ConvUnroll<WT, NJ, NJ> {
+template <int WT, int CV, int NJ>
+struct ConvUnroll<WT, CV, NJ, NJ> {
     __device__ static __forceinline__ void run(Ctx&, int, uint32_t) {}
 };
 
-template <int WT>
+template <int WT, int CV>
 __device__ __forceinline__ void converter_loop(Ctx& c, int nsuper) {
     using L = Smem<WT>;
     using B = Bars<WT>;
@@ -290,7 +293,7 @@ __device__ __forceinline__ void converter_loop(Ctx& c, int nsuper) {
             c.ok = false;
             return;
         }
-        ConvUnroll<WT, 0, SS>::run(c, t, c.sb + L::raw_off + rs * L::raw_slot);
+        ConvUnroll<WT, CV, 0, SS>::run(c, t, c.sb + L::raw_off + rs * L::raw_slot);
         __syncwarp();
         if ((threadIdx.x & 31) == 0) mbar_arrive(B::rempty(c, rs));
     }
@@ -346,14 +349,15 @@ __host__ __device__ __forceinline__ int tail_split(int T, int sms, int kparts, i
 // DBG: instead of the rescale, the epilogue stores every 32-k block's exact integer accumulator (the weights'
 // integer sub-scales folded in, as the converters fold them) to int32 [M][N][K/32] at `out`; dense, whole
 // K range per CTA.
-template <int WT, bool MOE, bool DBG = false>
-__global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
+template <int WT, bool MOE, bool DBG = false, int CV = default_conv<WT>()>
+__global__ void __launch_bounds__(Warps<WT, CV>::kThreads, 1)
     mmq_gemm_tma_kernel(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_xd, const __grid_constant__ CUtensorMap tm_xs,
                         float* __restrict__ out, int M, int N, int K, int ntn, int nfull, int lgp,
                         const MoeTiles moe) {
     using L = Smem<WT>;
     using B = Bars<WT>;
+    using W = Warps<WT, CV>;
     constexpr int U = Geom<WT>::U, UG = Geom<WT>::UG, SS = Geom<WT>::SS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -411,18 +415,18 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     c.ok = true;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
 
-    if (warp == Warps<WT>::kMma) {
+    if (warp == W::kMma) {
         if (lane == 0) {
             for (int i = 0; i < Ring<WT>::kStages; i++) {
-                mbar_init(B::full(c, i), Warps<WT>::kConv + 1);     // converter warps + the B load
+                mbar_init(B::full(c, i), W::kConv + 1);     // converter warps + the B load
                 mbar_init(B::empty(c, i), 1);
             }
             for (int i = 0; i < RAW_SLOTS; i++) {
                 mbar_init(B::rfull(c, i), 1);
-                mbar_init(B::rempty(c, i), Warps<WT>::kConv);
+                mbar_init(B::rempty(c, i), W::kConv);
             }
             for (int i = 0; i < SC; i++) {
-                mbar_init(B::sfull(c, i), Warps<WT>::kConv + 1);    // converter warps + the scale load
+                mbar_init(B::sfull(c, i), W::kConv + 1);    // converter warps + the scale load
                 mbar_init(B::sfree(c, i), EPI_WARPS);
             }
             for (int i = 0; i < NSB; i++) {
@@ -436,7 +440,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         __syncwarp();
         tmem_alloc(smem_u32(tmem_slot), NACC * BN);
         tmem_relinquish();
-    } else if (warp == Warps<WT>::kLoad && lane == 0) {
+    } else if (warp == W::kLoad && lane == 0) {
         tma_prefetch_desc(&tm_raw);
         tma_prefetch_desc(&tm_b);
         tma_prefetch_desc(&tm_xd);
@@ -447,7 +451,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == Warps<WT>::kLoad) {
+    if (warp == W::kLoad) {
         // =========================================================== TMA loader
         if (lane == 0) {
             for (int s = 0; s < nstages; s++) {
@@ -475,11 +479,11 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= Warps<WT>::kConv0 && warp < Warps<WT>::kMma) {
+    } else if (warp >= W::kConv0 && warp < W::kMma) {
         // =========================================================== converters
-        c.pt = (warp - Warps<WT>::kConv0) * 32 + lane;
-        converter_loop<WT>(c, nstages / SS);
-    } else if (warp == Warps<WT>::kMma) {
+        c.pt = (warp - W::kConv0) * 32 + lane;
+        converter_loop<WT, CV>(c, nstages / SS);
+    } else if (warp == W::kMma) {
         // =========================================================== MMA issuer
         const uint32_t idesc = idesc_f16_f32(BM, BN);
         const uint32_t a_smem = c.sb + L::a_off;
@@ -658,7 +662,7 @@ __global__ void __launch_bounds__(Warps<WT>::kThreads, 1)
         }
     }
     tc_fence_after();
-    if (warp == Warps<WT>::kMma) tmem_dealloc(tmem_base, NACC * BN);
+    if (warp == W::kMma) tmem_dealloc(tmem_base, NACC * BN);
 }
 
 }  // namespace tma

@@ -96,7 +96,8 @@ def test_quantizer_extreme_scales_bit_exact():
 
 # ---------------------------------------------------------------------------------------- block GEMM
 SHAPES = [(1, 1, 256), (5, 130, 256), (130, 257, 512), (200, 300, 1024), (256, 384, 2048), (64, 128, 5376),
-          (20, 1, 1024), (9, 3, 256)]           # the last two: tile path (M > 8) with one and three weight rows
+          (20, 1, 1024), (9, 3, 256),           # tile path (M > 8) with one and three weight rows
+          (64, 300, 1024), (65, 300, 1024)]     # either side of the four-converter kernel for <= 64 tokens
 
 
 @pytest.mark.parametrize("wtype", BLOCK_TYPES)
