@@ -370,17 +370,25 @@ def main():
     # replayed every step, so the device times are not host submission times (every kernel runs again on
     # every replay; the L2 flush stays an eager launch between steps).  --eager times the API calls.
     run_quant, run_gemm = quant_call, gemm_call
+    timed_as = "API calls issued eagerly"
     if not args.eager:
         def capture(fn):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 fn()
             return g
-        g_gemm = capture(gemm_call)
-        run_gemm = g_gemm.replay
-        if wt != synth.W8A8:
-            g_quant = capture(quant_call)
-            run_quant = g_quant.replay
+        try:
+            g_gemm = capture(gemm_call)
+            g_quant = capture(quant_call) if wt != synth.W8A8 else None
+        except RuntimeError as exc:     # keep the measurement: time the eager calls and say why
+            print(f"bench: CUDA-graph capture failed ({exc}); timing eager calls", file=sys.stderr)
+            torch.cuda.synchronize()
+            timed_as = f"API calls issued eagerly (graph capture failed: {str(exc)[:120]})"
+        else:
+            run_gemm = g_gemm.replay
+            if g_quant is not None:
+                run_quant = g_quant.replay
+            timed_as = "CUDA-graph replay of each leg (quantize; GEMM), every kernel re-run per step"
         for _ in range(2):
             flush.zero_()
             run_quant()
@@ -513,8 +521,7 @@ def main():
             "scaling": "weak", "vs_baseline": None,
             "dtype": "s8 x s8 -> exact block dot (fp16 tensor cores, f32 accumulate), f32 rescale",
             "data": "synthetic",
-            "config": dict(workload_config(name), timed_as="API calls issued eagerly" if args.eager else
-                           "CUDA-graph replay of each leg (quantize; GEMM), every kernel re-run per step"),
+            "config": dict(workload_config(name), timed_as=timed_as),
             "tok_per_s": job_throughput(tokens, world, K_steps, dev_total),
             "pct_int8_peak": (100.0 * value / world / int8_peak) if int8_peak else None,
             "int8_peak_tops": int8_peak,
