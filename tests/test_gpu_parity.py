@@ -128,6 +128,47 @@ def test_few_token_path_bit_exact(wtype, shape):
     assert np.array_equal(out.view(np.uint32), ref.view(np.uint32)), np.abs(out - ref).max()
 
 
+def _extreme_fields(wtype, N, K, g):
+    """Weight fields at the ends of their ranges, alternating sign by row and by value."""
+    f = synth.draw_fields(g, wtype, N, K)
+    alt = (np.arange(N)[:, None] + np.arange(K)[None, :]) % 2 == 0
+    if wtype == synth.Q8_0:
+        f.q[...] = np.where(alt, 127, -127).astype(np.int8)
+    elif wtype == synth.Q4_0:
+        f.code[...] = np.where(alt, 0, 15).astype(np.uint8)         # -8 and +7
+    elif wtype == synth.Q4_K:
+        f.code[...] = 15
+        f.sc[...] = 63
+        f.m[...] = 63
+    elif wtype == synth.IQ1_M:
+        f.g[...] = np.where(alt, 1, -1).astype(np.int8)
+        f.s[...] = 7
+    elif wtype == synth.Q6_K:
+        f.code[...] = np.where(alt, 0, 63).astype(np.uint8)         # -32 and +31
+        f.sc[...] = np.where(np.arange(K // 16)[None, :] % 2 == 0, -128, 127).astype(np.int8)
+    return f
+
+
+@pytest.mark.parametrize("wtype", BLOCK_TYPES)
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_few_token_path_bit_exact_at_the_bounds(wtype, M):
+    # weight and activation codes at the ends of their ranges (every in-block dot at or near its largest
+    # magnitude), random scales: the matrix-vector kernel stays bit-identical to the oracle
+    if wtype == synth.Q6_K and M > 4:
+        pytest.skip("q6_K takes the matrix-vector kernel up to 4 tokens")
+    N, K = 67, 2048
+    g = np.random.default_rng(41 + wtype + M)
+    W = synth.pack(wtype, _extreme_fields(wtype, N, K, g))
+    q = np.where(g.integers(0, 2, size=(M, K)) == 0, -127, 127).astype(np.int8)
+    q[0] = 127
+    d = g.uniform(1e-3, 1e-2, size=(M, K // 32)).astype(np.float32)
+    s = (d * q.reshape(M, K // 32, 32).sum(-1, dtype=np.int32).astype(np.float32)).astype(np.float32)
+    xq = api.pack_q8_1(torch.from_numpy(q), torch.from_numpy(d), torch.from_numpy(s)).to(DEV)
+    out = api.gemm(wtype, _dev(W.reshape(-1)), xq, M, N, K).cpu().numpy()
+    ref = oracle.gemm(wtype, W, q, d, s, N)
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32)), np.abs(out - ref).max()
+
+
 @pytest.mark.parametrize("wtype", [synth.Q6_K, synth.Q4_K])
 def test_small_grid_k_parts_at_super_stage_boundaries(wtype):
     # 2 tiles on a 152-SM part: every tile runs in 16 K parts; K = 11008 has 43 super-stages, so the
