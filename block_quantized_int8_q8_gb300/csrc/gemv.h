@@ -5,10 +5,11 @@
 
 namespace mmq {
 
-// Largest token count the matrix-vector kernel takes; larger M run on the tile kernels.  q6_K's decode is
-// the heaviest per value: from 5 tokens on its tile path is faster (measured on the 7B FFN-down shape).
+// Largest token count the matrix-vector kernel takes; larger M run on the tile kernels (every type: q6_K,
+// the heaviest decode per value, still beats its tile path at 5-7 tokens and ties it at 8 on the 7B
+// FFN-down shape).
 constexpr int MMVQ_MAX_M = 8;
-inline int mmvq_max_m(int wt) { return wt == 5 /* q6_K */ ? 4 : MMVQ_MAX_M; }
+inline int mmvq_max_m(int) { return MMVQ_MAX_M; }
 
 // out f32 [M][N] for block-type weights W (raw blocks, N rows of row_bytes) and q8_1 activations Xq
 // (int8 codes [M][K] at byte 0, float2 (d, s) [M][K/32] at byte M*K); 1 <= M <= MMVQ_MAX_M, K % 256 == 0.

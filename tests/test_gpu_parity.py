@@ -115,12 +115,10 @@ def test_block_gemm_matches_oracle(wtype, shape):
 @pytest.mark.parametrize("shape", [(1, 1, 256), (3, 130, 1280), (8, 257, 4096), (5, 64, 768), (4, 200, 11008),
                                    (2, 40001, 256), (7, 3, 512)])
 def test_few_token_path_bit_exact(wtype, shape):
-    # M <= 8 (q6_K: 4) runs on the matrix-vector kernel, which forms every block term and sum in the
+    # M <= 8 runs on the matrix-vector kernel, which forms every block term and sum in the
     # blockwise definition's order: the f32 output equals the oracle's bit for bit (K = 1280, 768 and
     # 11008 leave a partial chunk of 32-value blocks; 40001 rows outnumber one pass of the grid)
     M, N, K = shape
-    if wtype == synth.Q6_K and M > 4:
-        pytest.skip("q6_K takes the matrix-vector kernel up to 4 tokens")
     pb = synth.make_problem(wtype, M, N, K, seed=13 + M + N + wtype)
     q, d, s, xq = _oracle_acts(pb)
     out = api.gemm(wtype, _dev(pb.W.reshape(-1)), xq, M, N, K).cpu().numpy()
@@ -154,8 +152,6 @@ def _extreme_fields(wtype, N, K, g):
 def test_few_token_path_bit_exact_at_the_bounds(wtype, M):
     # weight and activation codes at the ends of their ranges (every in-block dot at or near its largest
     # magnitude), random scales: the matrix-vector kernel stays bit-identical to the oracle
-    if wtype == synth.Q6_K and M > 4:
-        pytest.skip("q6_K takes the matrix-vector kernel up to 4 tokens")
     N, K = 67, 2048
     g = np.random.default_rng(41 + wtype + M)
     W = synth.pack(wtype, _extreme_fields(wtype, N, K, g))
