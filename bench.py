@@ -368,7 +368,8 @@ def main():
     assert api.read_device_errors() == 0
     # Each leg (quantize; GEMM, MoE routing and gather included) is captured once as a CUDA graph and
     # replayed every step, so the device times are not host submission times (every kernel runs again on
-    # every replay; the L2 flush stays an eager launch between steps).  --eager times the API calls.
+    # every replay; the L2 flush stays an eager launch between steps).  --eager times the API calls.  The mode is the
+    # line's "timing" field.
     run_quant, run_gemm = quant_call, gemm_call
     timed_as = "API calls issued eagerly"
     if not args.eager:
@@ -521,7 +522,7 @@ def main():
             "scaling": "weak", "vs_baseline": None,
             "dtype": "s8 x s8 -> exact block dot (fp16 tensor cores, f32 accumulate), f32 rescale",
             "data": "synthetic",
-            "config": dict(workload_config(name), timed_as=timed_as),
+            "config": workload_config(name), "timing": timed_as,
             "tok_per_s": job_throughput(tokens, world, K_steps, dev_total),
             "pct_int8_peak": (100.0 * value / world / int8_peak) if int8_peak else None,
             "int8_peak_tops": int8_peak,
