@@ -105,13 +105,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -463,7 +456,7 @@ __global__ void __launch_bounds__(Warps<WT, CV>::kThreads, 1)
                         tma_load_2d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, (t + s0 / SS) * UG * 16, wrow,
                                     B::rfull(c, rs));
                     else
-                        tma_load_3d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, 0, (t + s0 / SS) * UG, wrow,
+                        tma_load_2d(c.sb + L::raw_off + rs * L::raw_slot, &tm_raw, (t + s0 / SS) * UG * 4, wrow,
                                     B::rfull(c, rs));
                 }
                 const int slot = s % Ring<WT>::kStages;
