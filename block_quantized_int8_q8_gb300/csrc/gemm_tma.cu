@@ -75,7 +75,8 @@ cudaError_t launch(const TmaGemmArgs& a, cudaStream_t stream, bool dbg) {
         // one 2-D box of whole row chunks: bytes where the chunk fits a box dimension (256 elements),
         // else 4-byte elements (Q8_0 272 B, IQ1_M 304 B per row; row strides and chunk offsets are
         // multiples of 16 bytes).  A box of 16-byte units along a third dimension lands the same bytes in
-        // the same place but as many more, smaller TMA requests: measured 2x slower from a cold L2.
+        // the same place but as many more, smaller TMA requests (measured: the 64x256x1024 Q8_0 GEMM 14 %
+        // slower, IQ1_M 1-4 % slower).
         const bool words = U * 16 > 256;
         const cuuint64_t dims[2] = {(cuuint64_t)(words ? a.w_row_bytes / 4 : a.w_row_bytes), (cuuint64_t)wrows};
         const cuuint64_t strides[1] = {(cuuint64_t)a.w_row_bytes};
