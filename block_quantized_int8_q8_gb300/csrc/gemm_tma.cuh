@@ -10,8 +10,9 @@
 //     1024 k) for the 128 rows, into a two-slot raw ring; (b) the token operand, fp16 codes of the
 //     q8_1 shadow, 64 k x 128 tokens with the 128-byte swizzle straight into the MMA operand ring;
 //     (c) the tokens' block scales d (Q4_K also s) from the block-major shadow into a scale ring.
-//   * a converter group (two warps; four for IQ1_M and q6_K): each thread takes two weight rows in one
-//     unrolled body (one row for IQ1_M and q6_K), reads its raw bytes from the raw ring (16-byte loads,
+//   * a converter group (two warps; four for IQ1_M and q6_K, and for every type on dense grids of at
+//     most 64 tokens): each thread takes two weight rows in one unrolled body (one row with four warps),
+//     reads its raw bytes from the raw ring (16-byte loads,
 //     conflict-free: the row pitch is an odd number of 16-byte units), unpacks them EXACTLY to fp16
 //     integers (the unpackers of gemm.cuh; q6_K's below), stores the 128B-swizzled K-major operand row
 //     (q6_K: two rows, its sub-block scale split over two exact operands) and the row's block scales.
