@@ -14,45 +14,25 @@
 using namespace mmq;
 
 namespace {
-
-constexpr long long kMaxDim = (1ll << 31) - 1;
-
 thread_local char g_last_cuda_error[256] = "";
+}  // namespace
 
-// Record a CUDA failure for mmq_last_cuda_error and map it to the ABI status.
-mmq_status cuda_fail(cudaError_t e, const char* where) {
+namespace mmq {
+mmq_status record_cuda_failure(cudaError_t e, const char* where) {
     snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s)", where, cudaGetErrorName(e),
              cudaGetErrorString(e));
     return MMQ_ERR_CUDA;
 }
+}  // namespace mmq
+
+namespace {
+
+mmq_status cuda_fail(cudaError_t e, const char* where) { return record_cuda_failure(e, where); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-long long weight_row_bytes(mmq_type t, long long K) {
-    switch (t) {
-        case MMQ_Q8_0: return K / 32 * 34;
-        case MMQ_Q4_0: return K / 32 * 18;
-        case MMQ_Q4_K: return K / 256 * 144;
-        case MMQ_IQ1_M: return K / 256 * 76;
-        case MMQ_W8A8: return K;
-        case MMQ_Q6_K: return K / 256 * 224;
-    }
-    return -1;
-}
-
-bool known_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_Q6_K; }
-bool block_type(int t) { return (t >= MMQ_Q8_0 && t <= MMQ_IQ1_M) || t == MMQ_Q6_K; }
-// Types the general kernel takes (debug partials, mmq_gemm_id_noalloc, shapes the TMA kernel does not).
-bool general_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_W8A8; }
-
-// Shape rules shared by every GEMM entry point.
-mmq_status check_shape(mmq_type t, long long M, long long N, long long K) {
-    if (M < 0 || N < 0 || K <= 0) return MMQ_ERR_SHAPE;
-    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return MMQ_ERR_SHAPE;
-    if (M * K > kMaxDim || N * K > kMaxDim) return MMQ_ERR_SHAPE;
-    if (t == MMQ_W8A8) return (K % 64 == 0) ? MMQ_OK : MMQ_ERR_SHAPE;
-    return (K % 256 == 0) ? MMQ_OK : MMQ_ERR_SHAPE;
-}
+long long weight_row_bytes(mmq_type t, long long K) { return mmq::weight_row_bytes((int)t, K); }
+mmq_status check_shape(mmq_type t, long long M, long long N, long long K) { return mmq::check_shape((int)t, M, N, K); }
 
 cudaError_t dispatch(mmq_type t, const GemmParams& p, int mode, bool moe, int grid_y, cudaStream_t s) {
     switch (t) {
@@ -78,7 +58,6 @@ GemmParams dense_params(mmq_type t, const void* W, const void* Xq, void* out, lo
         const Q81Layout L = q81_layout(M, K);
         p.xds = reinterpret_cast<const float4*>(xb + L.ds);
         p.xh = reinterpret_cast<const uint16_t*>(xb + L.h);
-        p.xs3 = reinterpret_cast<const uint4*>(xb + L.xs3);
     }
     p.out = out;
     p.w_row_bytes = weight_row_bytes(t, K);
@@ -140,25 +119,23 @@ const char* mmq_status_string(mmq_status s) {
 }
 
 size_t mmq_q8_1_bytes(int64_t M, int64_t K) {
-    if (M < 0 || K < 0 || K % 64 != 0) return 0;
+    if (!q8_1_shape_ok(M, K)) return 0;                    // exactly where mmq_quantize_q8_1 says MMQ_ERR_SHAPE
     return (size_t)q81_layout(M, K).total;
 }
 
 size_t mmq_weight_bytes(mmq_type t, int64_t N, int64_t K) {
-    if (!known_type(t) || N < 0 || K <= 0) return 0;
-    if (block_type(t) && (t == MMQ_Q4_K || t == MMQ_IQ1_M || t == MMQ_Q6_K) && K % 256 != 0) return 0;
-    if (K % 32 != 0) return 0;
+    if (!known_type(t) || check_shape(t, 0, N, K) != MMQ_OK) return 0;   // exactly where mmq_gemm says MMQ_ERR_SHAPE
     if (t == MMQ_W8A8) return (size_t)(N * K + 4 * N);
     return (size_t)(N * weight_row_bytes(t, K));
 }
 
 size_t mmq_w8a8_act_bytes(int64_t M, int64_t K) {
-    if (M < 0 || K < 0) return 0;
+    if (check_shape(MMQ_W8A8, M, 0, K) != MMQ_OK) return 0;
     return (size_t)(M * K + 4 * M);
 }
 
 mmq_status mmq_q8_1_prepare(void* xq, int64_t M, int64_t K, mmq_stream_t stream) {
-    if (M < 0 || K <= 0 || K % 64 != 0 || M * K > kMaxDim) return MMQ_ERR_SHAPE;
+    if (!q8_1_shape_ok(M, K)) return MMQ_ERR_SHAPE;
     if (M == 0) return MMQ_OK;
     if (!xq) return MMQ_ERR_INVALID_ARG;
     if (!aligned16(xq)) return MMQ_ERR_ALIGN;
@@ -167,7 +144,7 @@ mmq_status mmq_q8_1_prepare(void* xq, int64_t M, int64_t K, mmq_stream_t stream)
 }
 
 mmq_status mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, void* xq, mmq_stream_t stream) {
-    if (M < 0 || K <= 0 || K % 64 != 0 || M * K > kMaxDim) return MMQ_ERR_SHAPE;
+    if (!q8_1_shape_ok(M, K)) return MMQ_ERR_SHAPE;
     if (M == 0) return MMQ_OK;
     if (!x || !xq) return MMQ_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xq)) return MMQ_ERR_ALIGN;

@@ -2,13 +2,57 @@
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
+#include "../../include/mmq.h"
 
 namespace mmq {
 struct GemmParams;
 
+// ------------------------------------------------------------------------------------------ shape rules
+// One set of rules for every entry point and size helper (include/mmq.h, "Shape rules").
+constexpr long long kMaxDim = (1ll << 31) - 1;
+
+inline bool known_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_Q6_K; }
+inline bool block_type(int t) { return (t >= MMQ_Q8_0 && t <= MMQ_IQ1_M) || t == MMQ_Q6_K; }
+// Types the general kernel takes (debug partials, mmq_gemm_id_noalloc, shapes the TMA kernel does not).
+inline bool general_type(int t) { return t >= MMQ_Q8_0 && t <= MMQ_W8A8; }
+
+// K granule of a weight type: the block types run in 256-k super-stages, W8A8 in 64-k stages.
+inline long long k_granule(int t) { return t == MMQ_W8A8 ? 64 : 256; }
+
+// Raw bytes of one weight row of K values (-1 for an unknown type).
+inline long long weight_row_bytes(int t, long long K) {
+    switch (t) {
+        case MMQ_Q8_0: return K / 32 * 34;
+        case MMQ_Q4_0: return K / 32 * 18;
+        case MMQ_Q4_K: return K / 256 * 144;
+        case MMQ_IQ1_M: return K / 256 * 76;
+        case MMQ_W8A8: return K;
+        case MMQ_Q6_K: return K / 256 * 224;
+    }
+    return -1;
+}
+
+// Shape rules shared by every GEMM entry point: M, N >= 0; K > 0 and a multiple of the type's granule;
+// M*K and N*K below 2^31.
+inline mmq_status check_shape(int t, long long M, long long N, long long K) {
+    if (M < 0 || N < 0 || K <= 0) return MMQ_ERR_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return MMQ_ERR_SHAPE;
+    if (M * K > kMaxDim || N * K > kMaxDim) return MMQ_ERR_SHAPE;
+    return (K % k_granule(t) == 0) ? MMQ_OK : MMQ_ERR_SHAPE;
+}
+
+// q8_1 activation buffers (the quantizer's rule): K > 0, K % 64 == 0, M*K below 2^31.
+inline bool q8_1_shape_ok(long long M, long long K) {
+    return M >= 0 && K > 0 && K % 64 == 0 && M <= kMaxDim && M * K <= kMaxDim;
+}
+
+// Record a CUDA failure for mmq_last_cuda_error (the calling host thread's message) and return
+// MMQ_ERR_CUDA (capi.cu).
+mmq_status record_cuda_failure(cudaError_t e, const char* where);
+
 // q8_1 buffer sections (byte offsets), see include/mmq.h
 struct Q81Layout {
-    long long ds, h, xs3, dT, sT, Mp, total;
+    long long ds, h, dT, sT, Mp, total;
 };
 inline Q81Layout q81_layout(long long M, long long K) {
     Q81Layout L;
@@ -16,8 +60,7 @@ inline Q81Layout q81_layout(long long M, long long K) {
     L.Mp = (M + 3) / 4 * 4;                       // block-major rows padded to 16 bytes
     L.ds = M * K;
     L.h = (M * K + M * kb * 8 + 255) / 256 * 256;
-    L.xs3 = L.h + 2 * M * K;
-    L.dT = (L.xs3 + M * kb * 16 + 255) / 256 * 256;
+    L.dT = (L.h + 2 * M * K + 255) / 256 * 256;
     L.sT = L.dT + L.Mp * kb * 4;
     L.total = (L.sT + L.Mp * kb * 4 + 255) / 256 * 256;
     return L;

@@ -11,6 +11,9 @@
 // call's contents; the routing kernels rewrite every entry they later read (the per-expert counts
 // are cleared at the start of each call), so nothing has to be zero on entry.  Two calls whose
 // kernels overlap on the GPU (different streams, no ordering between them) race on the array.
+// The array's device address is looked up once per device and kept for the life of the process: it
+// assumes the device's primary context, which the CUDA runtime uses, is never torn down and recreated
+// (cudaDeviceReset) while the library is in use.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -47,16 +50,6 @@ cudaError_t scratch_for_current_device(void** out) {
     return cudaSuccess;
 }
 
-long long row_bytes(mmq_type t, long long K) {
-    switch (t) {
-        case MMQ_Q8_0: return K / 32 * 34;
-        case MMQ_Q4_0: return K / 32 * 18;
-        case MMQ_Q4_K: return K / 256 * 144;
-        case MMQ_IQ1_M: return K / 256 * 76;
-        default: return -1;
-    }
-}
-
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
@@ -64,10 +57,14 @@ size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_experts, const void* Xq,
                                           const int32_t* expert_ids, int n_slots, float* out, int64_t M,
                                           int64_t N, int64_t K, mmq_stream_t stream) {
-    if (wtype < MMQ_Q8_0 || wtype > MMQ_IQ1_M) return wtype == MMQ_W8A8 ? MMQ_ERR_UNSUPPORTED : MMQ_ERR_INVALID_ARG;
+    if (!known_type(wtype)) return MMQ_ERR_INVALID_ARG;
+    // the general kernel's block types; W8A8 has no MoE form and Q6_K runs on the TMA-fed kernel only
+    if (!block_type(wtype) || !general_type(wtype)) return MMQ_ERR_UNSUPPORTED;
     if (n_experts <= 0 || n_slots <= 0) return MMQ_ERR_INVALID_ARG;
-    if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return MMQ_ERR_SHAPE;
-    if (M * K >= (1ll << 31) || N * K >= (1ll << 31) || M * n_slots >= (1ll << 31)) return MMQ_ERR_SHAPE;
+    const mmq_status st = check_shape(wtype, M, N, K);
+    if (st != MMQ_OK) return st;
+    if (M * n_slots > kMaxDim || (long long)n_experts * N * weight_row_bytes(wtype, K) > (1ll << 40))
+        return MMQ_ERR_SHAPE;
     if (M == 0 || N == 0) return MMQ_OK;
     if (!W || !Xq || !expert_ids || !out) return MMQ_ERR_INVALID_ARG;
     auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -82,7 +79,8 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
     if (total > MMQ_NOALLOC_SCRATCH_BYTES) return MMQ_ERR_WORKSPACE;   // problem too large for the array
 
     void* base = nullptr;
-    if (scratch_for_current_device(&base) != cudaSuccess) return MMQ_ERR_CUDA;
+    cudaError_t e = scratch_for_current_device(&base);
+    if (e != cudaSuccess) return record_cuda_failure(e, "mmq_gemm_id_noalloc scratch address");
     uint8_t* sb = static_cast<uint8_t*>(base);
     RouteWorkspace ws;
     ws.counts = reinterpret_cast<int*>(sb + counts);
@@ -93,7 +91,8 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
     ws.rowlist = reinterpret_cast<int*>(sb + rowlist);
     ws.max_work = max_work;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s) != cudaSuccess) return MMQ_ERR_CUDA;
+    e = run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s);
+    if (e != cudaSuccess) return record_cuda_failure(e, "mmq_gemm_id_noalloc routing");
 
     GemmParams p{};
     p.W = static_cast<const uint8_t*>(W);
@@ -101,9 +100,8 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
     const Q81Layout Lq = q81_layout(M, K);
     p.xds = reinterpret_cast<const float4*>(static_cast<const uint8_t*>(Xq) + Lq.ds);
     p.xh = reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(Xq) + Lq.h);
-    p.xs3 = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(Xq) + Lq.xs3);
     p.out = out;
-    p.w_row_bytes = row_bytes(wtype, K);
+    p.w_row_bytes = weight_row_bytes(wtype, K);
     p.w_expert_bytes = p.w_row_bytes * N;
     p.M = (int)M;
     p.N = (int)N;
@@ -112,7 +110,7 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
     p.work = ws.work;
     p.nwork = ws.nwork;
     p.slots = n_slots;
-    cudaError_t e = cudaErrorInvalidValue;
+    e = cudaErrorInvalidValue;
     switch (wtype) {
         case MMQ_Q8_0: e = run_gemm_q8_0(p, MODE_PROD, true, max_work, s); break;
         case MMQ_Q4_0: e = run_gemm_q4_0(p, MODE_PROD, true, max_work, s); break;
@@ -120,5 +118,5 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
         case MMQ_IQ1_M: e = run_gemm_iq1_m(p, MODE_PROD, true, max_work, s); break;
         default: break;
     }
-    return e == cudaSuccess ? MMQ_OK : MMQ_ERR_CUDA;
+    return e == cudaSuccess ? MMQ_OK : record_cuda_failure(e, "mmq_gemm_id_noalloc");
 }

@@ -23,15 +23,15 @@
  *     a device-resident error word that mmq_read_device_errors() returns and clears.
  *
  * Byte layouts (this library's; the pages give block sizes, not bit layouts):
- *   q8_1 activations (mmq_q8_1_bytes(M,K) bytes), four sections:
+ *   q8_1 activations (mmq_q8_1_bytes(M,K) bytes), five sections:
  *       int8 q[M][K]                    at byte 0            the q8_1 codes
  *       float2 ds[M][K/32] = (d, s)     at byte M*K          per-block scale and block sum
  *       fp16 h[M][K]                    at byte H = round_up(M*K + 8*M*K/32, 256)
  *                                                            h = q exactly (tensor-core operand)
- *       bf16 xs3[M][K/32][8]            at byte H + 2*M*K    per block {x1,x1,x2,x2,x3,x3,0,0}
- *                                                            with x1 + x2 + x3 = d exactly (x1, x2 are
- *                                                            d and its remainder truncated to bf16)
- *       The first two sections are the q8_1 blocks (40 B per 32 values); the last two are derived
+ *       f32 dT[K/32][Mp], sT[K/32][Mp]  at byte T = round_up(H + 2*M*K, 256) and T + 4*Mp*K/32,
+ *                                                            Mp = M rounded up to 4: d and s
+ *                                                            block-major (the GEMM's 128-token boxes)
+ *       The first two sections are the q8_1 blocks (40 B per 32 values); the last three are derived
  *       from them (mmq_q8_1_prepare) so that the GEMM reads tensor-core-ready operands.
  *   Q8_0  34 B / 32 values : f16 d | int8 q[32]                        value = d*q
  *   Q4_0  18 B / 32 values : f16 d | 16 B, byte i = code i (low nibble) | code i+16 (high nibble)
@@ -55,10 +55,14 @@
  *   W8A8 activations       : int8 X[M][K] followed by f32 xs[M]        (mmq_w8a8_act_bytes)
  *   Weights are row-major over N: row n is its K/values-per-block blocks back to back.
  *
- * Shape rules: M >= 1, N >= 1 (any value; tails are masked).  K >= 256 and K % 256 == 0 for the block
- * types (Q8_0, Q4_0, Q4_K, IQ1_M, Q6_K); K % 64 == 0 for W8A8.  M*K and N*K below 2^31.
+ * Shape rules: M >= 0, N >= 0 (any value; tails are masked; M == 0 or N == 0 is a no-op).  K > 0 and
+ * K % 256 == 0 for the block types (Q8_0, Q4_0, Q4_K, IQ1_M, Q6_K: the kernels stage raw weights in
+ * 256-value super-stages); K % 64 == 0 for W8A8 and for q8_1 activation buffers (64-value stages).
+ * M*K and N*K below 2^31.  Every size helper returns 0 for exactly the shapes its entry point rejects
+ * with MMQ_ERR_SHAPE (mmq_weight_bytes: mmq_gemm's rule for the type; mmq_q8_1_bytes:
+ * mmq_quantize_q8_1's; mmq_w8a8_act_bytes: W8A8's).
  * Q6_K runs on the TMA-fed kernel only: mmq_gemm and mmq_gemm_id take it; mmq_gemm_debug_partials
- * returns MMQ_ERR_UNSUPPORTED and mmq_gemm_id_noalloc MMQ_ERR_INVALID_ARG for it.
+ * and mmq_gemm_id_noalloc return MMQ_ERR_UNSUPPORTED for it (as they do for W8A8).
  */
 #ifndef MMQ_GB300_H
 #define MMQ_GB300_H
@@ -104,13 +108,14 @@ const char* mmq_status_string(mmq_status s);
  * host thread ("" if none).  The string stays valid until the next failing call on that thread. */
 const char* mmq_last_cuda_error(void);
 
-/* Bytes of a q8_1 activation buffer for an [M][K] matrix, all four sections (K % 64 == 0). */
+/* Bytes of a q8_1 activation buffer for an [M][K] matrix, all sections (0 unless K > 0, K % 64 == 0). */
 size_t mmq_q8_1_bytes(int64_t M, int64_t K);
 
-/* Bytes of a raw weight buffer of type t with N rows of K values (W8A8: N*K + 4*N). 0 on bad args. */
+/* Bytes of a raw weight buffer of type t with N rows of K values (W8A8: N*K + 4*N).  0 for an unknown
+ * type or a shape mmq_gemm rejects (K % 256 for the block types, K % 64 for W8A8). */
 size_t mmq_weight_bytes(mmq_type t, int64_t N, int64_t K);
 
-/* Bytes of a W8A8 activation buffer: M*K + 4*M. */
+/* Bytes of a W8A8 activation buffer: M*K + 4*M (0 unless K > 0, K % 64 == 0). */
 size_t mmq_w8a8_act_bytes(int64_t M, int64_t K);
 
 /*
@@ -119,14 +124,14 @@ size_t mmq_w8a8_act_bytes(int64_t M, int64_t K);
  * xq  : output q8_1 buffer of mmq_q8_1_bytes(M, K) bytes, device.
  * Per row and 32-value block: amax = max|x|; d = amax/127 (f32, round to nearest); q = round-half-even
  * of the correctly rounded f32 x/d, clamped to [-127,127]; s = d*(float)sum(q).  amax == 0 gives
- * d = 0, q = 0, s = 0.  Inputs must be finite.  K % 64 == 0.  Writes all four sections.
+ * d = 0, q = 0, s = 0.  Inputs must be finite.  K % 64 == 0.  Writes all five sections.
  */
 mmq_status mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, void* xq, mmq_stream_t stream);
 
 /*
- * mmq_q8_1_prepare -- fill the two derived sections (h, xs3) of a q8_1 buffer from its q and ds
+ * mmq_q8_1_prepare -- fill the derived sections (h, dT, sT) of a q8_1 buffer from its q and ds
  * sections, for callers that produce q8_1 blocks themselves.  mmq_quantize_q8_1 already does this.
- * Exact: h = q as fp16; x1 = d truncated to bf16, x2 = (d - x1) truncated to bf16, x3 = d - x1 - x2.
+ * Exact: h = q as fp16; dT, sT are d and s transposed (pad columns up to Mp zero).
  */
 mmq_status mmq_q8_1_prepare(void* xq, int64_t M, int64_t K, mmq_stream_t stream);
 

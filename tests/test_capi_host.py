@@ -29,7 +29,9 @@ def test_header_declares_exactly_the_exported_api(lib):
 def test_sizes(lib):
     o = api.q8_1_offsets(3, 64)
     assert o["ds"] == 3 * 64 and o["h"] % 256 == 0 and o["h"] >= 3 * 64 + 3 * 2 * 8
-    assert api.q8_1_bytes(3, 64) >= o["xs3"] + 3 * 2 * 16 and api.q8_1_bytes(3, 64) % 256 == 0
+    assert o["dT"] >= o["h"] + 3 * 64 * 2 and o["dT"] % 256 == 0 and o["sT"] == o["dT"] + 4 * 2 * 4
+    assert api.q8_1_bytes(3, 64) == (o["sT"] + 4 * 2 * 4 + 255) // 256 * 256
+    assert api.q8_1_bytes(3, 64) == int(api.load().mmq_q8_1_bytes(3, 64))
     assert api.q8_1_bytes(3, 32) == 0                     # K % 64 required
     assert api.weight_bytes(api.Q8_0, 5, 256) == 5 * 8 * 34
     assert api.weight_bytes(api.Q4_0, 5, 256) == 5 * 8 * 18
@@ -44,6 +46,24 @@ def test_sizes(lib):
 
 
 FAKE = 1 << 20          # 16-byte aligned, never dereferenced: every case fails validation first
+
+
+@pytest.mark.parametrize("K", [32, 64, 96, 128, 256, 288, 512, 1024, 0, -256])
+def test_size_helpers_agree_with_the_entry_points(lib, K):
+    """A size helper returns 0 exactly where its entry point rejects the shape: with a null pointer the
+    entry point answers MMQ_ERR_SHAPE (2) for a bad K and MMQ_ERR_INVALID_ARG (1) once the shape passes,
+    so no kernel is ever launched here."""
+    for t in (api.Q8_0, api.Q4_0, api.Q4_K, api.IQ1_M, api.W8A8, api.Q6_K):
+        st = lib.mmq_gemm(t, None, FAKE, FAKE, 4, 4, K, None)
+        assert st in (1, 2), (t, K, st)
+        assert (api.weight_bytes(t, 4, K) == 0) == (st == 2), (t, K)
+        if t != api.W8A8:
+            sid = lib.mmq_gemm_id(t, None, 2, FAKE, FAKE, 2, FAKE, 4, 4, K, FAKE, 1 << 30, None)
+            assert sid == st, (t, K, sid)
+    sq = lib.mmq_quantize_q8_1(None, 4, K, FAKE, None)
+    assert sq in (1, 2)
+    assert (api.q8_1_bytes(4, K) == 0) == (sq == 2), K
+    assert (api.w8a8_act_bytes(4, K) == 0) == (lib.mmq_gemm(api.W8A8, None, FAKE, FAKE, 4, 4, K, None) == 2), K
 
 
 @pytest.mark.parametrize("args,status", [
@@ -74,6 +94,11 @@ def test_quantize_and_gemm_id_validation(lib):
     assert lib.mmq_gemm_debug_partials(api.Q4_K, FAKE, FAKE, FAKE, 4, 4, 128, None) == 2
     assert lib.mmq_gemm_debug_partials(api.Q6_K, FAKE, FAKE, FAKE, 4, 4, 256, None) == 4   # TMA kernel only
     assert lib.mmq_gemm(6, FAKE, FAKE, FAKE, 4, 4, 256, None) == 1                         # unknown type
+    # the no-allocation MoE entry point: types it does not implement, and its shape rules
+    for t in (api.W8A8, api.Q6_K):
+        assert lib.mmq_gemm_id_noalloc(t, FAKE, 4, FAKE, FAKE, 2, FAKE, 16, 128, 256, None) == 4
+    assert lib.mmq_gemm_id_noalloc(api.Q4_0, FAKE, 4, FAKE, FAKE, 2, FAKE, 16, 128, 96, None) == 2
+    assert lib.mmq_gemm_id_noalloc(api.Q4_0, None, 4, FAKE, FAKE, 2, FAKE, 16, 128, 256, None) == 1
     for s in range(7):
         assert lib.mmq_status_string(s)
     assert lib.mmq_read_device_errors(None, None) == 1
