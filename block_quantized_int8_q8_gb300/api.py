@@ -123,9 +123,8 @@ def q8_1_offsets(M: int, K: int) -> dict:
     Mp = (M + 3) // 4 * 4
     ds = M * K
     h = (M * K + M * kb * 8 + 255) // 256 * 256
-    xs3 = h + 2 * M * K
-    dT = (xs3 + M * kb * 16 + 255) // 256 * 256
-    return {"q": 0, "ds": ds, "h": h, "xs3": xs3, "dT": dT, "sT": dT + Mp * kb * 4, "Mp": Mp}
+    dT = (h + 2 * M * K + 255) // 256 * 256
+    return {"q": 0, "ds": ds, "h": h, "dT": dT, "sT": dT + Mp * kb * 4, "Mp": Mp}
 
 
 def q8_1_views(buf: torch.Tensor, M: int, K: int):
@@ -137,15 +136,13 @@ def q8_1_views(buf: torch.Tensor, M: int, K: int):
 
 
 def q8_1_shadow_views(buf: torch.Tensor, M: int, K: int):
-    """(h fp16 [M, K], xs3 bf16 [M, K/32, 8], dT f32 [K/32, M], sT f32 [K/32, M]) views of a q8_1
-    buffer's derived sections."""
+    """(h fp16 [M, K], dT f32 [K/32, M], sT f32 [K/32, M]) views of a q8_1 buffer's derived sections."""
     o = q8_1_offsets(M, K)
     kb, Mp = K // 32, o["Mp"]
     h = buf[o["h"]: o["h"] + 2 * M * K].view(torch.float16).view(M, K)
-    xs3 = buf[o["xs3"]: o["xs3"] + M * kb * 16].view(torch.bfloat16).view(M, kb, 8)
     dT = buf[o["dT"]: o["dT"] + Mp * kb * 4].view(torch.float32).view(kb, Mp)[:, :M]
     sT = buf[o["sT"]: o["sT"] + Mp * kb * 4].view(torch.float32).view(kb, Mp)[:, :M]
-    return h, xs3, dT, sT
+    return h, dT, sT
 
 
 def q8_1_prepare(buf: torch.Tensor, M: int, K: int, stream=None) -> torch.Tensor:

@@ -51,6 +51,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// bf16 record {x1, x1, x2, x2, x3, x3, 0, 0} with x1 + x2 + x3 = d exactly: x1 keeps d's top 16 bits,
+// x2 those of the remainder, and the last remainder has at most 8 significant bits.
+__device__ __forceinline__ uint4 split3_record(float d) {
+    const float x1 = __uint_as_float(__float_as_uint(d) & 0xFFFF0000u);
+    const float r1 = __fsub_rn(d, x1);
+    const float x2 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
+    const float x3 = __fsub_rn(r1, x2);
+    const uint32_t h1 = __float_as_uint(x1) >> 16, h2 = __float_as_uint(x2) >> 16, h3 = __float_as_uint(x3) >> 16;
+    return make_uint4(h1 | (h1 << 16), h2 | (h2 << 16), h3 | (h3 << 16), 0u);
+}
+
 // bf16 record {w1, w2, w1, w2, w1, w2, 0, 0} with w1 + w2 = v exactly (v has at most 16 significant
 // bits: an f16 scale, halved); w1 keeps v's top 16 bits.
 __device__ __forceinline__ uint4 split2_record(float v) {
@@ -87,7 +98,6 @@ struct GemmParams {
     const uint8_t* W;           // raw weights (expert 0 for MoE); W8A8: int8 [N][K]
     const int8_t* xq;           // activation codes [M][K]
     const float4* xds;          // q8_1 (d, s) pairs [M][K/32], read two blocks at a time
-    const uint4* xs3;           // q8_1 shadow: bf16 pieces of d per block [M][K/32]
     const float* w8_ws;         // W8A8 per-channel scales [N]
     const float* w8_xs;         // W8A8 per-token scales [M]
     const uint16_t* xh;         // q8_1 shadow: fp16 codes [M][K] (block types)
@@ -127,7 +137,7 @@ template <int WT, bool SB, bool RING>
 struct SmemLayoutT {
     static constexpr bool kW8 = WT == WT_W8A8;
     static constexpr int raw_b = kW8 ? BN * 64 : 0;              // int8 codes per token row
-    static constexpr int raw_ds = RING ? BN * 16 : 0;            // (d, s) of the stage's two blocks
+    static constexpr int raw_ds = (SB || RING) ? BN * 16 : 0;    // (d, s) of the stage's two blocks
     static constexpr int raw_a = BM * RawGeom<WT>::kStride;
     static constexpr int raw_stage = (raw_b + raw_ds + raw_a + 127) / 128 * 128;
     static constexpr int sop_block = (BM + BN) * 16;             // weight-side then token-side scale rows
@@ -470,13 +480,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
 #pragma unroll
                 for (int k = 0; k < 8; k++)
                     cp_async_16(bt + 2048 * k, b_src[k] + 128 * s, ((b_ok >> k) & 1) ? 16u : 0u);
-                if constexpr (T::kSB) {                         // token-side scale rows of the two blocks
-                    const uint4* src = p.xs3 + my_row * kb32 + 2 * s;
-                    const uint32_t so = sop_smem + slot * SmemLayout::sop_stage + BM * 16 + 16 * pt;
-                    cp_async_16(so, src, my_ok ? 16u : 0u);
-                    cp_async_16(so + SmemLayout::sop_block, src + 1, my_ok ? 16u : 0u);
-                }
-                if constexpr (T::kScaleRing) {                  // (d, s) of the stage's two blocks
+                if constexpr (T::kSB || T::kScaleRing) {        // (d, s) of the stage's two blocks
                     const uint8_t* src = xds_bytes + (my_row * kb32 + 2 * s) * 8;
                     cp_async_16(rb + 16 * pt, src, my_ok ? 16u : 0u);
                 }
@@ -537,12 +541,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) mmq_gemm_kernel(const GemmParams 
                     st_shared_v4(at + sw128_off(pt, c), ha[4 * c], ha[4 * c + 1], ha[4 * c + 2], ha[4 * c + 3]);
                 if constexpr (T::kSB) {
                     // weight-side scale rows {w1,w2,w1,w2,w1,w2,0,0}, w1 + w2 = wd/2 (the MMA counts
-                    // every product twice)
+                    // every product twice), and this thread's token row's {x1,x1,x2,x2,x3,x3,0,0},
+                    // x1 + x2 + x3 = d, from the staged (d, s) pairs of the two blocks
                     const uint32_t so = sop_smem + slot * SmemLayout::sop_stage + 16 * pt;
+                    const float4 dsx = ld_shared_f4(rb + 16 * pt);
 #pragma unroll
                     for (int i = 0; i < 2; i++) {
                         const uint4 rec = split2_record(0.5f * wsc[i]);
                         st_shared_v4(so + i * SmemLayout::sop_block, rec.x, rec.y, rec.z, rec.w);
+                        const uint4 tr = split3_record(i == 0 ? dsx.x : dsx.z);
+                        st_shared_v4(so + i * SmemLayout::sop_block + BM * 16, tr.x, tr.y, tr.z, tr.w);
                     }
                 }
                 if constexpr (T::kScaleRing) {

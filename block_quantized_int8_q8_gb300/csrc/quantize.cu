@@ -4,10 +4,11 @@
 // division), s = d * sum(q)  ("08 · R1 — int8 MMQ prefill GEMM", §2.2 q8_1 activation pipeline, and
 // the §3.2 reference quantizer; f32 scale, the block sum produced in the same pass).
 // Output layout (include/mmq.h): int8 q[M][K], float2 (d, s)[M][K/32], then the tensor-core shadow:
-// fp16 h[M][K] = q exactly, bf16 {x1,x1,x2,x2,x3,x3,0,0} per block with x1 + x2 + x3 = d exactly,
-// and the block-major copies d^T, s^T [K/32][Mp] that the TMA-fed GEMM loads per 128-token tile.
+// fp16 h[M][K] = q exactly, and the block-major copies d^T, s^T [K/32][Mp] that the TMA-fed GEMM loads
+// per 128-token tile.
 //
-// HBM-bound: 4 bytes read and 1.25 bytes written per value.  Eight lanes own one block (one float4
+// HBM-bound: 4 bytes read per value; 1.25 bytes of q8_1 blocks and 2.25 bytes of shadow (fp16 codes,
+// block-major scales) written.  Eight lanes own one block (one float4
 // each); amax and sum(q) are warp-shuffle reductions over the eight lanes; every lane stores its
 // four codes as one 32-bit word, so a warp writes 128 contiguous bytes per block quad.
 #include <cstdint>
@@ -26,17 +27,6 @@ __device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
     return v;
 }
 
-// d = x1 + x2 + x3 exactly, each a bf16: x1 keeps d's top 16 bits, x2 the remainder's top 16 bits,
-// and the last remainder has at most 8 significant bits.  Returned as the 16-byte block record.
-__device__ __forceinline__ uint4 split3_record(float d) {
-    const float x1 = __uint_as_float(__float_as_uint(d) & 0xFFFF0000u);
-    const float r1 = __fsub_rn(d, x1);
-    const float x2 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
-    const float x3 = __fsub_rn(r1, x2);
-    const uint32_t h1 = __float_as_uint(x1) >> 16, h2 = __float_as_uint(x2) >> 16, h3 = __float_as_uint(x3) >> 16;
-    return make_uint4(h1 | (h1 << 16), h2 | (h2 << 16), h3 | (h3 << 16), 0u);
-}
-
 // four codes -> four fp16 (exact)
 __device__ __forceinline__ uint2 codes_to_f16x4(int q0, int q1, int q2, int q3) {
     const __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
@@ -51,7 +41,7 @@ __device__ __forceinline__ int q8_code(float x, float d) {
 
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, uint32_t* __restrict__ q,
                                                            float2* __restrict__ ds, uint2* __restrict__ h,
-                                                           uint4* __restrict__ xs3, float* __restrict__ dT,
+                                                           float* __restrict__ dT,
                                                            float* __restrict__ sT, int kb, long long Mp,
                                                            long long nblk) {
     const int lane = threadIdx.x & 31, sub = lane & 7, grp = lane >> 3;
@@ -91,7 +81,6 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
                 if (sub == 0) {
                     const float sv = __fmul_rn(d, (float)sum);
                     ds[blk] = make_float2(d, sv);
-                    xs3[blk] = split3_record(d);
                     const long long m = blk / kb, b = blk - m * kb;
                     dT[b * Mp + m] = d;
                     sT[b * Mp + m] = sv;
@@ -119,15 +108,15 @@ cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq
     const Q81Layout L = q81_layout(M, K);
     quantize_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(
         reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(base), reinterpret_cast<float2*>(base + L.ds),
-        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3),
-        reinterpret_cast<float*>(base + L.dT), reinterpret_cast<float*>(base + L.sT), (int)(K / 32), L.Mp, nblk);
+        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<float*>(base + L.dT),
+        reinterpret_cast<float*>(base + L.sT), (int)(K / 32), L.Mp, nblk);
     return cudaGetLastError();
 }
 
 // Derived sections from existing q8_1 blocks: eight lanes per block, one 32-bit word of codes each.
 __global__ void __launch_bounds__(256) prepare_q8_1_kernel(const uint32_t* __restrict__ q,
                                                           const float2* __restrict__ ds, uint2* __restrict__ h,
-                                                          uint4* __restrict__ xs3, float* __restrict__ dT,
+                                                          float* __restrict__ dT,
                                                           float* __restrict__ sT, int kb, long long Mp,
                                                           long long nblk) {
     const long long stride = (gridDim.x * (long long)blockDim.x) >> 3;
@@ -138,7 +127,6 @@ __global__ void __launch_bounds__(256) prepare_q8_1_kernel(const uint32_t* __res
                                           (int)(int8_t)((w >> 16) & 0xff), (int)(int8_t)(w >> 24));
         if (sub == 0) {
             const float2 v = ds[blk];
-            xs3[blk] = split3_record(v.x);
             const long long m = blk / kb, b = blk - m * kb;
             dT[b * Mp + m] = v.x;
             sT[b * Mp + m] = v.y;
@@ -162,8 +150,8 @@ cudaError_t run_prepare_q8_1(void* xq, long long M, long long K, cudaStream_t s)
     const Q81Layout L = q81_layout(M, K);
     prepare_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(
         reinterpret_cast<const uint32_t*>(base), reinterpret_cast<const float2*>(base + L.ds),
-        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<uint4*>(base + L.xs3),
-        reinterpret_cast<float*>(base + L.dT), reinterpret_cast<float*>(base + L.sT), (int)(K / 32), L.Mp, nblk);
+        reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<float*>(base + L.dT),
+        reinterpret_cast<float*>(base + L.sT), (int)(K / 32), L.Mp, nblk);
     return cudaGetLastError();
 }
 
