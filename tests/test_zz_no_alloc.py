@@ -44,6 +44,26 @@ def test_noalloc_matches_workspace_entry_point_twice(wtype, M, E, slots, N, K):
     assert _rel(second, ref) <= TOL
 
 
+@pytest.mark.parametrize("wtype", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.IQ1_M])
+def test_noalloc_larger_call_then_smaller_call(wtype):
+    # the shared array keeps the previous call's lists: a larger problem (more experts, more rows) run
+    # first must not leak into a smaller one with a different expert count run right after
+    N, K = 136, 1024
+    big = synth.make_problem(wtype, 90, N, K, seed=201, experts=24, slots=4)
+    small = synth.make_problem(wtype, 17, N, K, seed=202, experts=5, slots=2)
+    dev = "cuda"
+    for pb in (big, small):
+        pb.Wd = torch.from_numpy(pb.W.reshape(-1)).to(dev)
+        pb.xq = api.quantize_q8_1(torch.from_numpy(pb.x).to(dev))
+        pb.idsd = torch.from_numpy(pb.ids).to(dev)
+    ref_small = api.gemm_id(wtype, small.Wd, small.experts, small.xq, small.idsd, small.M, N, K)
+    api.gemm_id_noalloc(wtype, big.Wd, big.experts, big.xq, big.idsd, big.M, N, K)
+    got_small = api.gemm_id_noalloc(wtype, small.Wd, small.experts, small.xq, small.idsd, small.M, N, K)
+    torch.cuda.synchronize()
+    assert api.read_device_errors() == 0
+    assert _rel(got_small, ref_small) <= TOL
+
+
 def test_noalloc_rejects_problems_beyond_the_scratch_array():
     M, E, slots, N, K = 300000, 4, 1, 128, 256
     assert M * slots * 4 > api.NOALLOC_SCRATCH_BYTES       # the rowlist alone exceeds the array
