@@ -276,6 +276,142 @@ def workload_config(name):
 
 
 # ------------------------------------------------------------------------------------------ GPU arm
+# ------------------------------------------------------------------------------------------ GPU legs
+def setup_workload(name, dev, eager, warmup, flush):
+    """Inputs, output and the two legs (quantize; GEMM with MoE routing and gather) of one workload on
+    the device, warmed up and, unless eager, captured as CUDA graphs that are replayed every step (every
+    kernel runs again on every replay; the L2 flush stays an eager launch between steps)."""
+    import torch
+    from block_quantized_int8_q8_gb300 import api
+    pb = synth.workload(name)
+    wt = pb.wtype
+    M, N, K = pb.M, pb.N, pb.K
+    ops, tokens = workload_ops(name)
+    W = torch.from_numpy(pb.W.reshape(-1)).to(dev)
+    is_moe = pb.ids is not None
+    xq = ids = ws = None
+    if wt == synth.W8A8:
+        x = torch.from_numpy(synth.pack_w8a8_acts(pb.X, pb.xs)).to(dev)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        launches_per_step = 1
+    else:
+        x = torch.from_numpy(pb.x).to(dev)
+        xq = torch.empty(api.q8_1_bytes(M, K), dtype=torch.uint8, device=dev)
+        if is_moe:
+            ids = torch.from_numpy(pb.ids).to(dev)
+            out = torch.empty((M, pb.ids.shape[1], N), dtype=torch.float32, device=dev)
+            ws = torch.empty(api.gemm_id_workspace_bytes(M, K, pb.ids.shape[1], pb.experts), dtype=torch.uint8,
+                             device=dev)
+            # quantize, routing (one single-block launch up to 65536 rows and 1024 experts, else four),
+            # operand gather, grouped GEMM
+            small = M * pb.ids.shape[1] <= 65536 and pb.experts <= 1024
+            moe_tma = K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
+            launches_per_step = (4 if small else 7) if moe_tma else 6
+        else:
+            out = torch.empty((M, N), dtype=torch.float32, device=dev)
+            # quantize, GEMM (plus the zeroing of the K-split tail tiles' rows on the tile path)
+            launches_per_step = 2
+
+    def gemm_call(xin=None, o=None):
+        xin = x if xin is None else xin
+        o = out if o is None else o
+        if wt == synth.W8A8:
+            api.gemm(wt, W, xin, M, N, K, out=o)
+        elif is_moe:
+            api.gemm_id(wt, W, pb.experts, xq, ids, M, N, K, out=o, workspace=ws)
+        else:
+            api.gemm(wt, W, xq, M, N, K, out=o)
+
+    def quant_call(xin=None):
+        if wt != synth.W8A8:
+            api.quantize_q8_1(x if xin is None else xin, out=xq)
+
+    for _ in range(warmup):
+        flush.zero_()
+        quant_call()
+        gemm_call()
+    torch.cuda.synchronize()
+    assert api.read_device_errors() == 0
+    run_quant, run_gemm = quant_call, gemm_call
+    timed_as = "API calls issued eagerly"
+    if not eager:
+        def capture(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            return g
+        try:
+            g_gemm = capture(gemm_call)
+            g_quant = capture(quant_call) if wt != synth.W8A8 else None
+        except RuntimeError as exc:     # keep the measurement: time the eager calls and say why
+            print(f"bench: CUDA-graph capture failed ({exc}); timing eager calls", file=sys.stderr)
+            torch.cuda.synchronize()
+            timed_as = f"API calls issued eagerly (graph capture failed: {str(exc)[:120]})"
+        else:
+            run_gemm = g_gemm.replay
+            if g_quant is not None:
+                run_quant = g_quant.replay
+            timed_as = "CUDA-graph replay of each leg (quantize; GEMM), every kernel re-run per step"
+        for _ in range(2):
+            flush.zero_()
+            run_quant()
+            run_gemm()
+        torch.cuda.synchronize()
+        assert api.read_device_errors() == 0
+    tma_path = wt != synth.W8A8 and K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
+    kernel = "mmq_w8a8_tma_kernel" if wt == synth.W8A8 else ("mmq_gemm_tma_kernel" if tma_path else "mmq_gemm_kernel")
+    if wt != synth.W8A8 and not is_moe and M <= 8:
+        kernel = "mmvq_kernel"
+    return dict(pb=pb, wt=wt, M=M, N=N, K=K, ops=ops, tokens=tokens, x=x, out=out, quant_call=quant_call,
+                gemm_call=gemm_call, run_quant=run_quant, run_gemm=run_gemm, timed_as=timed_as,
+                launches_per_step=launches_per_step, kernel=kernel)
+
+
+def timed_steps(wl, steps, flush, stream):
+    """`steps` timed steps (L2 flush, quantize leg, GEMM leg), CUDA events on the launching stream;
+    per-step (step, GEMM, quantize) milliseconds."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        wl["run_quant"]()
+        ev[i][1].record(stream)
+        wl["run_gemm"]()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(steps)]
+    gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+    quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+    return step_ms, gemm_ms, quant_ms
+
+
+def workloads_block(dev, stream, flush, steps, warmup, peak, eager, gpu_id):
+    """Every workload of the suite (the five configurations, W8A8 at both token counts, the dense IQ1_M
+    shape and q6_K) timed with the headline's protocol, `steps` steps each."""
+    import torch
+    from block_quantized_int8_q8_gb300 import api
+    res = {}
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    tw0 = time.time()
+    for name in synth.WORKLOADS:
+        wl = setup_workload(name, dev, eager, warmup, flush)
+        step_ms, gemm_ms, quant_ms = timed_steps(wl, steps, flush, stream)
+        errs = api.read_device_errors()
+        step = statistics.mean(step_ms) / 1e3
+        gemm = statistics.mean(gemm_ms) / 1e3
+        res[name] = {"config": workload_config(name), "kernel": wl["kernel"],
+                     "step_tops": wl["ops"] / step / 1e12, "gemm_only_tops": wl["ops"] / gemm / 1e12,
+                     "step_ms": step * 1e3, "gemm_ms": gemm * 1e3, "quantize_ms": statistics.mean(quant_ms),
+                     "tok_per_s": wl["tokens"] / step, "frac_of_peak": wl["ops"] / gemm / 1e12 / peak,
+                     "steps": steps, "device_errors": errs}
+        del wl
+        torch.cuda.empty_cache()
+    sampler.mark(tw0, time.time())
+    return res, sampler.stop()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -284,6 +420,8 @@ def main():
     ap.add_argument("--impl", choices=["mmq", "reference"], default="mmq")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="q4_0_7b")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--workload-steps", type=int, default=100,
+                    help="timed steps per workload of the 'workloads' block (0: leave the block out)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
@@ -317,89 +455,16 @@ def main():
     api.load()
 
     name = args.workload
-    pb = synth.workload(name)
-    wt = pb.wtype
-    M, N, K = pb.M, pb.N, pb.K
-    ops, tokens = workload_ops(name)
-    W = torch.from_numpy(pb.W.reshape(-1)).to(dev)
-    stream = torch.cuda.current_stream()
-    is_moe = pb.ids is not None
-    if wt == synth.W8A8:
-        x = torch.from_numpy(synth.pack_w8a8_acts(pb.X, pb.xs)).to(dev)
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        launches_per_step = 1
-    else:
-        x = torch.from_numpy(pb.x).to(dev)
-        xq = torch.empty(api.q8_1_bytes(M, K), dtype=torch.uint8, device=dev)
-        if is_moe:
-            ids = torch.from_numpy(pb.ids).to(dev)
-            out = torch.empty((M, pb.ids.shape[1], N), dtype=torch.float32, device=dev)
-            ws = torch.empty(api.gemm_id_workspace_bytes(M, K, pb.ids.shape[1], pb.experts), dtype=torch.uint8,
-                             device=dev)
-            # quantize, routing (one single-block launch up to 65536 rows and 1024 experts, else four),
-            # operand gather, grouped GEMM
-            small = M * pb.ids.shape[1] <= 65536 and pb.experts <= 1024
-            moe_tma = K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
-            launches_per_step = (4 if small else 7) if moe_tma else 6
-        else:
-            out = torch.empty((M, N), dtype=torch.float32, device=dev)
-            launches_per_step = 2           # quantize, GEMM
-
-    def gemm_call(xin=None, o=None):
-        xin = x if xin is None else xin
-        o = out if o is None else o
-        if wt == synth.W8A8:
-            api.gemm(wt, W, xin, M, N, K, out=o)
-        elif is_moe:
-            api.gemm_id(wt, W, pb.experts, xq, ids, M, N, K, out=o, workspace=ws)
-        else:
-            api.gemm(wt, W, xq, M, N, K, out=o)
-
-    def quant_call(xin=None):
-        if wt != synth.W8A8:
-            api.quantize_q8_1(x if xin is None else xin, out=xq)
-
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup):
-        flush.zero_()
-        quant_call()
-        gemm_call()
-    torch.cuda.synchronize()
-    assert api.read_device_errors() == 0
-    # Each leg (quantize; GEMM, MoE routing and gather included) is captured once as a CUDA graph and
-    # replayed every step, so the device times are not host submission times (every kernel runs again on
-    # every replay; the L2 flush stays an eager launch between steps).  --eager times the API calls.  The mode is the
-    # line's "timing" field.
-    run_quant, run_gemm = quant_call, gemm_call
-    timed_as = "API calls issued eagerly"
-    if not args.eager:
-        def capture(fn):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                fn()
-            return g
-        try:
-            g_gemm = capture(gemm_call)
-            g_quant = capture(quant_call) if wt != synth.W8A8 else None
-        except RuntimeError as exc:     # keep the measurement: time the eager calls and say why
-            print(f"bench: CUDA-graph capture failed ({exc}); timing eager calls", file=sys.stderr)
-            torch.cuda.synchronize()
-            timed_as = f"API calls issued eagerly (graph capture failed: {str(exc)[:120]})"
-        else:
-            run_gemm = g_gemm.replay
-            if g_quant is not None:
-                run_quant = g_quant.replay
-            timed_as = "CUDA-graph replay of each leg (quantize; GEMM), every kernel re-run per step"
-        for _ in range(2):
-            flush.zero_()
-            run_quant()
-            run_gemm()
-        torch.cuda.synchronize()
-        assert api.read_device_errors() == 0
+    stream = torch.cuda.current_stream()
+    wl = setup_workload(name, dev, args.eager, args.warmup, flush)
+    pb, wt, M, N, K = wl["pb"], wl["wt"], wl["M"], wl["N"], wl["K"]
+    ops, tokens = wl["ops"], wl["tokens"]
+    x, out, quant_call, gemm_call = wl["x"], wl["out"], wl["quant_call"], wl["gemm_call"]
+    timed_as, launches_per_step = wl["timed_as"], wl["launches_per_step"]
 
     # ---------------------------------------------------------------- timed region
     K_steps = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_steps)]
     sampler = ClockSampler(gpu_id_for_smi(torch, local))
     sampler.start()
     time.sleep(0.15)
@@ -408,22 +473,12 @@ def main():
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     tw0 = time.time()
-    for i in range(K_steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        run_quant()
-        ev[i][1].record(stream)
-        run_gemm()
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
+    step_ms, gemm_ms, quant_ms = timed_steps(wl, K_steps, flush, stream)
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - wall0
     sampler.mark(tw0, time.time())
     clocks = sampler.stop()
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K_steps)]
-    gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K_steps)]
-    quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K_steps)]
     dev_total = max_over_ranks(sum(step_ms) / 1e3, dev)
     errs = api.read_device_errors()
 
@@ -494,10 +549,9 @@ def main():
     gemm_avg = statistics.mean(gemm_ms) / 1e3
     achieved = ops / gemm_avg / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    # the block types run the TMA-fed kernel (dense and MoE; IQ1_M when K % 1024 == 0), W8A8 its own
-    # TMA-fed kernel; the remaining shapes run the general kernel
-    tma_path = wt != synth.W8A8 and K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
-    kernel = "mmq_w8a8_tma_kernel" if wt == synth.W8A8 else ("mmq_gemm_tma_kernel" if tma_path else "mmq_gemm_kernel")
+    # the block types run the TMA-fed kernel (dense and MoE; IQ1_M when K % 1024 == 0; the matrix-vector
+    # kernel for eight tokens or fewer), W8A8 its own TMA-fed kernel; the remaining shapes the general kernel
+    kernel = wl["kernel"]
     roofline = {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(name, kernel),
                 "peak_source": f"{peak_src} dense bf16 burst (fp16 operands, same nominal rate)",
@@ -524,9 +578,11 @@ def main():
             "data": "synthetic",
             "config": workload_config(name), "timing": timed_as,
             "tok_per_s": job_throughput(tokens, world, K_steps, dev_total),
-            "pct_int8_peak": (100.0 * value / world / int8_peak) if int8_peak else None,
-            "int8_peak_tops": int8_peak,
-            "int8_peak_source": "measured live: mma.sync.m16n8k32.s8, the only int8 tensor path on sm_103a",
+            # context, not the roofline: the GEMM runs on the fp16 tensor pipe (roofline above); this is the
+            # rate of the legacy warp-level int8 MMA, the only int8 tensor instruction sm_103a keeps
+            "legacy_int8_mma_sync": {"tops": int8_peak, "step_pct_of_it": (100.0 * value / world / int8_peak)
+                                     if int8_peak else None,
+                                     "source": "measured live: mma.sync.m16n8k32.s8 throughput probe"},
             "gemm_ms": statistics.mean(gemm_ms), "quantize_ms": statistics.mean(quant_ms),
             "gemm_only_tops": ops / gemm_avg / 1e12,
             "roofline": roofline,
@@ -535,6 +591,12 @@ def main():
             "wall_s": wall, "device_errors": errs}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the oracle baseline is a one-GPU figure
         line["cpu_baseline"] = cpu_baseline(pb, name, args.cpu_baseline_s)
+    if world == 1 and args.workload_steps > 0:
+        # every configuration, timed after the headline with the same protocol (one GPU)
+        del wl, x, out
+        torch.cuda.empty_cache()
+        line["workloads"], line["workloads_clocks"] = workloads_block(
+            dev, stream, flush, args.workload_steps, args.warmup, peak, args.eager, gpu_id_for_smi(torch, local))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
