@@ -35,6 +35,30 @@ from block_quantized_int8_q8_gb300 import synth  # noqa: E402
 
 METRIC = "effective int8 TOPS (2MNK/t) & prefill tok/s per type/shape; % of GB300 int8 peak"
 FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Leaves L2 (129 MB) cold between timed steps: writes a FLUSH_BYTES buffer, and in "write-read" mode
+    then reads a second one of the same size, so that the written buffer's dirty lines are written back
+    before the timed step starts instead of while it runs."""
+
+    def __init__(self, dev, mode):
+        import torch
+        self.mode = mode
+        self.wbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.rbuf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev) if mode == "write-read" else None
+
+    def __call__(self):
+        import torch
+        self.wbuf.zero_()
+        if self.rbuf is not None:
+            torch.amax(self.rbuf)
+
+    DESCRIBE = {"write-read": "flushed between timed steps (256 MiB write, then 256 MiB read: no dirty lines left)",
+                "write": "flushed between timed steps (256 MiB write)"}
+
+
+FLUSH_MODE = "write-read"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -269,7 +293,7 @@ def rescale_ceiling(wt, ops, ffma_tflops):
 def workload_config(name):
     w = synth.WORKLOADS[name]
     cfg = {"workload": name, "wtype": synth.TYPE_NAMES[w["wtype"]].upper(), "M_tokens": w["M"], "N": w["N"],
-           "K": w["K"], "seed": w["seed"], "l2": "flushed between timed steps (256 MiB write)"}
+           "K": w["K"], "seed": w["seed"], "l2": L2Flush.DESCRIBE[FLUSH_MODE]}
     if "experts" in w:
         cfg.update(experts=w["experts"], slots=w["slots"])
     return cfg
@@ -327,7 +351,7 @@ def setup_workload(name, dev, eager, warmup, flush):
             api.quantize_q8_1(x if xin is None else xin, out=xq)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         quant_call()
         gemm_call()
     torch.cuda.synchronize()
@@ -353,7 +377,7 @@ def setup_workload(name, dev, eager, warmup, flush):
                 run_quant = g_quant.replay
             timed_as = "CUDA-graph replay of each leg (quantize; GEMM), every kernel re-run per step"
         for _ in range(2):
-            flush.zero_()
+            flush()
             run_quant()
             run_gemm()
         torch.cuda.synchronize()
@@ -373,7 +397,7 @@ def timed_steps(wl, steps, flush, stream):
     import torch
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         wl["run_quant"]()
         ev[i][1].record(stream)
@@ -384,6 +408,50 @@ def timed_steps(wl, steps, flush, stream):
     gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
     quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
     return step_ms, gemm_ms, quant_ms
+
+
+def decode_stream(wl, dev, stream, replays=20):
+    """Few-token (M <= 8) weights as a decode pass sees them: R layers, each its own copy of the weight
+    matrix (R copies together at least twice the L2, so every layer's weights come from HBM), one CUDA graph
+    of R x (quantize, GEMM) replayed `replays` times between two CUDA events; and the same with the GEMMs
+    alone.  No flush is needed: each layer's weights are read once per pass and evicted by the others."""
+    import torch
+    from block_quantized_int8_q8_gb300 import api
+    pb, wt, M, N, K = wl["pb"], wl["wt"], wl["M"], wl["N"], wl["K"]
+    wbytes = wl["pb"].W.nbytes
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (132 << 20)
+    R = int(min(128, max(8, -(-(2 * l2) // wbytes))))
+    Ws = [torch.from_numpy(pb.W.reshape(-1)).to(dev) for _ in range(R)]
+    x, out = wl["x"], wl["out"]
+    xq = torch.empty(api.q8_1_bytes(M, K), dtype=torch.uint8, device=dev)
+
+    def layers(with_quant):
+        for W in Ws:
+            if with_quant:
+                api.quantize_q8_1(x, out=xq)
+            api.gemm(wt, W, xq, M, N, K, out=out)
+
+    res = {"layers": R, "weight_bytes_per_layer": wbytes, "replays": replays}
+    for key, wq in (("layer_us", True), ("gemm_us", False)):
+        layers(wq)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layers(wq)
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[key] = e0.elapsed_time(e1) * 1e3 / (replays * R)
+        del g
+    res["gemm_weight_GBps"] = wbytes / (res["gemm_us"] * 1e-6) / 1e9
+    del Ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def workloads_block(dev, stream, flush, steps, warmup, peak, eager, gpu_id):
@@ -420,6 +488,8 @@ def main():
     ap.add_argument("--impl", choices=["mmq", "reference"], default="mmq")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="q4_0_7b")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--flush", choices=["write", "write-read"], default="write-read",
+                    help="L2 flush between timed steps: a 256 MiB write, optionally followed by a 256 MiB read")
     ap.add_argument("--workload-steps", type=int, default=100,
                     help="timed steps per workload of the 'workloads' block (0: leave the block out)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -455,7 +525,9 @@ def main():
     api.load()
 
     name = args.workload
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    global FLUSH_MODE
+    FLUSH_MODE = args.flush
+    flush = L2Flush(dev, args.flush)
     stream = torch.cuda.current_stream()
     wl = setup_workload(name, dev, args.eager, args.warmup, flush)
     pb, wt, M, N, K = wl["pb"], wl["wt"], wl["M"], wl["N"], wl["K"]
@@ -591,6 +663,8 @@ def main():
             "wall_s": wall, "device_errors": errs}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the oracle baseline is a one-GPU figure
         line["cpu_baseline"] = cpu_baseline(pb, name, args.cpu_baseline_s)
+    if world == 1 and wl["kernel"] == "mmvq_kernel":
+        line["decode_stream"] = decode_stream(wl, dev, stream)
     if world == 1 and args.workload_steps > 0:
         # every configuration, timed after the headline with the same protocol (one GPU)
         del wl, x, out

@@ -2,14 +2,22 @@
 // byte once at memory speed instead of filling 128-token tensor-core tiles ("CUDA: add IQ1_M to MMQ":
 // small batches run on the matrix-vector path; the MMQ tiles win from ~100 tokens on).
 //
-// One warp per weight row.  The row is walked in chunks of 32 blocks of 32 values, one block per lane:
-// the warp stages the chunk's raw bytes in shared memory with coalesced cp.async copies, each lane decodes
-// its block to int8 words, forms the exact int32 block dot per token with dp4a ("08 · R1 — int8 MMQ
-// prefill GEMM", §2.1: the in-block integer dot is exact), and its f32 term u = (xd * wsc) * I
-// (Q4_K: minus dmin*m_b * s; IQ1_M and q6_K: one term per 16-value half).  Lane m then adds the chunk's
-// terms in block order into token m's running sum ("A Negative Result on int8 Tensor-Core MMQ", §2: the
+// One CTA of four warps per group of four weight rows.  Rows are walked in chunks of 32 blocks of 32 values
+// (one block per lane), four chunks (one per warp) at a time: each warp stages its chunk of every row in
+// shared memory with coalesced cp.async copies -- the whole segment of every row in flight at once --,
+// each lane decodes its block to int8 words, forms the exact int32 block dot per token with dp4a ("08 · R1 —
+// int8 MMQ prefill GEMM", §2.1: the in-block integer dot is exact), and its f32 term u = (xd * wsc) * I
+// (Q4_K: minus dmin*m_b * s; IQ1_M and q6_K: one term per 16-value half).  One thread per (row, token) then
+// adds the terms in block order into its running sum ("A Negative Result on int8 Tensor-Core MMQ", §2: the
 // blockwise contraction).  Every product and sum is a separate round-to-nearest step in the order written,
-// so the output is bit-identical to the blockwise definition computed in that order.
+// so the output is bit-identical to the blockwise definition computed in that order.  (One warp per row,
+// walking its chunks with two in flight, measured 2x slower at one token: two memory round trips per row.)
+//
+// Decode runs layer after layer, each a quantize launch and this kernel on a few hundred KB to tens of MB
+// of weights, so launch gaps matter: both kernels are launched as programmatic dependents.  This kernel's
+// CTAs start while the kernel before it finishes, pull their first row group's weights into L2 (a hint
+// with no effect on what loads return), and only then wait for the previous kernel's results; measured
+// on a stream of 7B-shaped Q4_0 layers at one token, quantize + GEMV per layer drops from 8.5 to 7.7 us.
 #include <cstdint>
 #include <cuda_fp16.h>
 #include "gemv.h"
@@ -19,7 +27,8 @@
 namespace mmq {
 namespace gemv {
 
-constexpr int WARPS = 4;                 // rows in flight per CTA (small CTAs balance the rows over the SMs)
+constexpr int WARPS = 4;                 // warps per CTA: one chunk of a segment each
+constexpr int RPC = 4;                   // weight rows per CTA
 constexpr int CHUNK = 32;                // 32-value blocks per chunk (one per lane)
 
 // Raw bytes of one chunk (32 blocks = 1024 values) per type.
@@ -27,11 +36,8 @@ __host__ __device__ constexpr int chunk_bytes(int wt) {
     return wt == WT_Q8_0 ? 32 * 34 : wt == WT_Q4_0 ? 32 * 18 : wt == WT_Q4_K ? 4 * 144 : wt == WT_IQ1_M ? 4 * 76 : 4 * 224;
 }
 __host__ __device__ constexpr bool per16(int wt) { return wt == WT_IQ1_M || wt == WT_Q6_K; }
-// A ring slot: one chunk plus one word that the last block's span read may touch, on 16-byte boundaries.
+// A staging slot: one chunk plus one word that the last block's span read may touch, on 16-byte boundaries.
 __host__ __device__ constexpr int stage_words(int wt) { return (chunk_bytes(wt) / 4 + 1 + 3) / 4 * 4; }
-// Ring slots per warp: DEPTH - 1 chunks in flight while one is decoded.  IQ1_M's chunks are the smallest
-// (304 B) and it gains from five slots at 4-8 tokens; the others measured best at three.
-__host__ __device__ constexpr int depth(int wt) { return wt == WT_IQ1_M ? 5 : 3; }
 
 // NW consecutive 32-bit words starting at byte offset o of the staged bytes (any alignment): NW + 1
 // aligned loads and a funnel shift each.
@@ -67,15 +73,16 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
         wsc[0] = wsc[1] = half_lo(b[0]);
 #pragma unroll
         for (int k = 0; k < 8; k++) w[k] = __funnelshift_r(b[k], b[k + 1], 16);
-    } else if constexpr (WT == WT_Q4_0) {          // f16 d | byte i = code i (low) | code i+16 (high)
+    } else if constexpr (WT == WT_Q4_0) {          // f16 d | byte i = code i (low) | code i+16 (high); codes
+                                                   // unsigned here, the kernel subtracts 8 * sum(q)
         uint32_t b[5];                             // bytes 18j .. 18j + 19
         st_span<5>(st, 18 * j, b);
         wsc[0] = wsc[1] = half_lo(b[0]);
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const uint32_t nw = __funnelshift_r(b[k], b[k + 1], 16);
-            w[k] = ((nw & 0x0F0F0F0Fu) + 0x78787878u) ^ 0x80808080u;         // code - 8 (see bias_byte)
-            w[4 + k] = (((nw >> 4) & 0x0F0F0F0Fu) + 0x78787878u) ^ 0x80808080u;
+            w[k] = nw & 0x0F0F0F0Fu;
+            w[4 + k] = (nw >> 4) & 0x0F0F0F0Fu;
         }
     } else if constexpr (WT == WT_Q4_K) {          // f16 d | f16 dmin | 12 B six-bit sc, m | 128 B codes
         const uint32_t* rec = st + 36 * (j >> 3);  // 144-byte records
@@ -129,104 +136,141 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
     }
 }
 
-// Grid-stride over weight rows, one row per warp at a time; MT tokens.  xq: int8 codes [MT][K];
-// xds: (d, s) [MT][K/32].  The row's chunks stream into a DEPTH-slot shared-memory ring with cp.async, so
-// DEPTH - 1 chunks of the weight stream are in flight while one is decoded.
+// CTA of WARPS warps per group of RPC weight rows (grid-stride over row groups); MT tokens.  xq: int8
+// codes [MT][K]; xds: (d, s) [MT][K/32].  A row is walked in segments of WARPS chunks: warp w copies chunk
+// w of the segment of every row of the group into shared memory (all of the segment's weight bytes in
+// flight at once: one memory round trip per segment instead of one per chunk), decodes its chunk's blocks
+// (one per lane) and writes each block's f32 term per row and token to shared memory.  Thread t < RPC*MT
+// then adds row t/MT's terms for token t%MT in block order, one dependent chain per (row, token).
 template <int WT, int MT>
 __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restrict__ W, long long row_bytes,
                                                         const int8_t* __restrict__ xq,
                                                         const float2* __restrict__ xds, float* __restrict__ out,
                                                         int N, int K) {
     constexpr int TPB = per16(WT) ? 2 : 1;        // terms per block
-    constexpr int DEPTH = depth(WT);
-    __shared__ __align__(16) uint32_t stage[WARPS][DEPTH][stage_words(WT)];
-    // row pitch 4 mod 32 words: the summing lanes' 16-byte reads fall in distinct banks
-    __shared__ __align__(16) float terms[WARPS][MT][TPB * CHUNK + 4];
+    constexpr int TSEG = WARPS * CHUNK * TPB;     // terms of one row and token per segment
+    static_assert(RPC * MT <= WARPS * 32, "one summing thread per (row, token)");
+    __shared__ __align__(16) uint32_t stage[RPC][WARPS][stage_words(WT)];
+    __shared__ __align__(16) float terms[RPC][MT][TSEG];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nb = K / 32, nchunks = (nb + CHUNK - 1) / CHUNK;
+    const int nb = K / 32, nchunks = (nb + CHUNK - 1) / CHUNK, nseg = (nchunks + WARPS - 1) / WARPS;
     const bool row16 = (row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(W) & 15) == 0;
-    for (long long n = (long long)blockIdx.x * WARPS + warp; n < N; n += (long long)gridDim.x * WARPS) {
-        const uint8_t* row = W + n * row_bytes;
-        // copy chunk c's raw words into ring slot c % DEPTH (one commit group per chunk, empty past the end)
-        // (16-byte copies that bypass L1 when the chunk allows it, so the weight stream does not evict the
-        // activations every row reads)
-        auto issue = [&](int c) {
-            if (c < nchunks) {
-                const int words = min(CHUNK, nb - c * CHUNK) * chunk_bytes(WT) / 128;   // whole words: K % 256 == 0
-                const uint8_t* src = row + (long long)c * chunk_bytes(WT);
-                const uint32_t dst = smem_u32(stage[warp][c % DEPTH]);
-                if (row16 && (words & 3) == 0) {
-                    for (int i = lane; i < words / 4; i += 32) cp_async_16(dst + 16 * i, src + 16 * i, 16);
-                } else {
-                    for (int i = lane; i < words; i += 32) cp_async_4(dst + 4 * i, src + 4 * i, 4);
+    const int sr = threadIdx.x / MT, sm = threadIdx.x % MT;   // summing thread: row sr, token sm
+    if ((long long)blockIdx.x * RPC < N) {
+        // the first row group's weights (contiguous rows) into L2 while the kernel before this one finishes
+        const long long n0 = (long long)blockIdx.x * RPC;
+        const long long bytes = min((long long)RPC, N - n0) * row_bytes;
+        const uint8_t* base = W + n0 * row_bytes;
+        for (long long o = (long long)threadIdx.x * 128; o < bytes; o += WARPS * 32 * 128) prefetch_l2(base + o);
+        if (threadIdx.x == 0) prefetch_l2(base + bytes - 1);
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (long long g = blockIdx.x; g * RPC < N; g += gridDim.x) {
+        const long long n0 = g * RPC;
+        const int rows = (int)min((long long)RPC, N - n0);
+        float acc = 0.0f;                          // row n0 + sr, token sm (threads below RPC * MT)
+        for (int sg = 0; sg < nseg; sg++) {
+            const int c = sg * WARPS + warp;       // this warp's chunk
+            const int nblk = c < nchunks ? min(CHUNK, nb - c * CHUNK) : 0;
+            if (nblk > 0) {
+                // every row's chunk c, 16-byte copies that bypass L1 where the rows allow it (the weight
+                // stream then does not evict the activations every row reads)
+                const int words = nblk * chunk_bytes(WT) / 128;              // whole words: K % 256 == 0
+#pragma unroll
+                for (int r = 0; r < RPC; r++) {
+                    if (r < rows) {
+                        const uint8_t* src = W + (n0 + r) * row_bytes + (long long)c * chunk_bytes(WT);
+                        const uint32_t dst = smem_u32(stage[r][warp]);
+                        if (row16 && (words & 3) == 0) {
+                            for (int i = lane; i < words / 4; i += 32) cp_async_16(dst + 16 * i, src + 16 * i, 16);
+                        } else {
+                            for (int i = lane; i < words; i += 32) cp_async_4(dst + 4 * i, src + 4 * i, 4);
+                        }
+                    }
                 }
             }
             cp_async_commit();
-        };
-        __syncwarp();                              // the previous row's last chunk is consumed
-#pragma unroll
-        for (int c = 0; c < DEPTH - 1; c++) issue(c);
-        float acc = 0.0f;                          // token `lane`'s running sum (lanes < MT)
-        for (int c = 0; c < nchunks; c++) {
-            issue(c + DEPTH - 1);                  // refills the slot chunk c - 1 used
-            cp_async_wait<DEPTH - 1>();            // this lane's copies of chunk c have landed
-            __syncwarp();                          // ... and every lane's
-            const uint32_t* st = stage[warp][c % DEPTH];
-            const int nblk = min(CHUNK, nb - c * CHUNK);
+            // the block's activations, every token, while the weights are in flight
+            int4 x0[MT], x1[MT];
+            float2 ds[MT];
             if (lane < nblk) {
                 const int b = c * CHUNK + lane;
-                int4 x0[MT], x1[MT];
-                float2 ds[MT];
 #pragma unroll
-                for (int m = 0; m < MT; m++) {     // every token's activation block in flight at once
+                for (int m = 0; m < MT; m++) {
                     const int4* xp = reinterpret_cast<const int4*>(xq + (long long)m * K + 32 * b);
                     x0[m] = __ldg(xp);
                     x1[m] = __ldg(xp + 1);
                     ds[m] = __ldg(xds + (long long)m * nb + b);
                 }
-                uint32_t w[8];
-                float wsc[2], wmin;
-                decode_block<WT>(st, lane, w, wsc, wmin);
+            }
+            // Q4_0 codes stay unsigned (0..15): the block dot is sum(code * q) - 8 * sum(q), exact in int32,
+            // with 8 * sum(q) formed once per token and shared by the group's rows
+            int sq8[MT];
 #pragma unroll
-                for (int m = 0; m < MT; m++) {
-                    int I0 = 0, I1 = 0;
-                    I0 = __dp4a((int)w[0], x0[m].x, I0);
-                    I0 = __dp4a((int)w[1], x0[m].y, I0);
-                    I0 = __dp4a((int)w[2], x0[m].z, I0);
-                    I0 = __dp4a((int)w[3], x0[m].w, I0);
-                    I1 = __dp4a((int)w[4], x1[m].x, I1);
-                    I1 = __dp4a((int)w[5], x1[m].y, I1);
-                    I1 = __dp4a((int)w[6], x1[m].z, I1);
-                    I1 = __dp4a((int)w[7], x1[m].w, I1);
-                    if constexpr (per16(WT)) {
-                        terms[warp][m][2 * lane] = __fmul_rn(__fmul_rn(ds[m].x, wsc[0]), (float)I0);
-                        terms[warp][m][2 * lane + 1] = __fmul_rn(__fmul_rn(ds[m].x, wsc[1]), (float)I1);
-                    } else {
-                        float u = __fmul_rn(__fmul_rn(ds[m].x, wsc[0]), (float)(I0 + I1));
-                        if constexpr (WT == WT_Q4_K) u = __fsub_rn(u, __fmul_rn(wmin, ds[m].y));
-                        terms[warp][m][lane] = u;
+            for (int m = 0; m < MT; m++) {
+                int t = 0;
+                if constexpr (WT == WT_Q4_0) {
+                    const int e8 = 0x08080808;
+                    t = __dp4a(e8, x0[m].x, t);
+                    t = __dp4a(e8, x0[m].y, t);
+                    t = __dp4a(e8, x0[m].z, t);
+                    t = __dp4a(e8, x0[m].w, t);
+                    t = __dp4a(e8, x1[m].x, t);
+                    t = __dp4a(e8, x1[m].y, t);
+                    t = __dp4a(e8, x1[m].z, t);
+                    t = __dp4a(e8, x1[m].w, t);
+                }
+                sq8[m] = t;
+            }
+            cp_async_wait<0>();
+            __syncwarp();                          // every lane's copies of the chunk have landed
+            if (lane < nblk) {
+#pragma unroll
+                for (int r = 0; r < RPC; r++) {
+                    if (r >= rows) break;
+                    uint32_t w[8];
+                    float wsc[2], wmin;
+                    decode_block<WT>(stage[r][warp], lane, w, wsc, wmin);
+#pragma unroll
+                    for (int m = 0; m < MT; m++) {
+                        int I0 = 0, I1 = WT == WT_Q4_0 ? -sq8[m] : 0;
+                        I0 = __dp4a((int)w[0], x0[m].x, I0);
+                        I0 = __dp4a((int)w[1], x0[m].y, I0);
+                        I0 = __dp4a((int)w[2], x0[m].z, I0);
+                        I0 = __dp4a((int)w[3], x0[m].w, I0);
+                        I1 = __dp4a((int)w[4], x1[m].x, I1);
+                        I1 = __dp4a((int)w[5], x1[m].y, I1);
+                        I1 = __dp4a((int)w[6], x1[m].z, I1);
+                        I1 = __dp4a((int)w[7], x1[m].w, I1);
+                        float* tp = &terms[r][m][(warp * CHUNK + lane) * TPB];
+                        if constexpr (per16(WT)) {
+                            tp[0] = __fmul_rn(__fmul_rn(ds[m].x, wsc[0]), (float)I0);
+                            tp[1] = __fmul_rn(__fmul_rn(ds[m].x, wsc[1]), (float)I1);
+                        } else {
+                            float u = __fmul_rn(__fmul_rn(ds[m].x, wsc[0]), (float)(I0 + I1));
+                            if constexpr (WT == WT_Q4_K) u = __fsub_rn(u, __fmul_rn(wmin, ds[m].y));
+                            tp[0] = u;
+                        }
                     }
                 }
             }
-            __syncwarp();
-            if (lane < MT) {                       // block order: the adds form one dependent chain
-                const int nt = TPB * nblk;
-                const float4* tp = reinterpret_cast<const float4*>(terms[warp][lane]);
-#pragma unroll
-                for (int q = 0; q < TPB * CHUNK / 4; q++) {
-                    if (4 * q < nt) {              // nt is a multiple of 8: K % 256 == 0
-                        const float4 v = tp[q];
-                        acc = __fadd_rn(acc, v.x);
-                        acc = __fadd_rn(acc, v.y);
-                        acc = __fadd_rn(acc, v.z);
-                        acc = __fadd_rn(acc, v.w);
-                    }
+            __syncthreads();                       // the segment's terms of every row are written
+            if (threadIdx.x < RPC * MT && sr < rows) {
+                // block order: chunk by chunk (warp order), block by block (lane order), halves in order
+                const float4* tp = reinterpret_cast<const float4*>(terms[sr][sm]);
+                const int nt = TPB * min(nb - sg * WARPS * CHUNK, WARPS * CHUNK);   // a multiple of 8
+                for (int q = 0; q < nt / 4; q++) {
+                    const float4 v = tp[q];
+                    acc = __fadd_rn(acc, v.x);
+                    acc = __fadd_rn(acc, v.y);
+                    acc = __fadd_rn(acc, v.z);
+                    acc = __fadd_rn(acc, v.w);
                 }
             }
-            __syncwarp();                          // chunk c's slot and terms are consumed
+            __syncthreads();                       // terms and staged chunks are consumed
         }
-        cp_async_wait<0>();
-        if (lane < MT) out[(long long)lane * N + n] = acc;
+        if (threadIdx.x < RPC * MT && sr < rows) out[(long long)sm * N + n0 + sr] = acc;
     }
 }
 
@@ -234,17 +278,16 @@ template <int WT>
 cudaError_t launch_m(dim3 g, dim3 b, cudaStream_t s, const uint8_t* w, long long row_bytes, const int8_t* xq,
                      const float2* xds, float* out, long long M, long long N, long long K) {
     switch (M) {
-        case 1: mmvq_kernel<WT, 1><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
-        case 2: mmvq_kernel<WT, 2><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
-        case 3: mmvq_kernel<WT, 3><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
-        case 4: mmvq_kernel<WT, 4><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
-        case 5: mmvq_kernel<WT, 5><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
-        case 6: mmvq_kernel<WT, 6><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
-        case 7: mmvq_kernel<WT, 7><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
-        case 8: mmvq_kernel<WT, 8><<<g, b, 0, s>>>(w, row_bytes, xq, xds, out, (int)N, (int)K); break;
+        case 1: return launch_pdl(mmvq_kernel<WT, 1>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 2: return launch_pdl(mmvq_kernel<WT, 2>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 3: return launch_pdl(mmvq_kernel<WT, 3>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 4: return launch_pdl(mmvq_kernel<WT, 4>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 5: return launch_pdl(mmvq_kernel<WT, 5>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 6: return launch_pdl(mmvq_kernel<WT, 6>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 7: return launch_pdl(mmvq_kernel<WT, 7>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 8: return launch_pdl(mmvq_kernel<WT, 8>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace gemv
@@ -255,8 +298,8 @@ cudaError_t run_gemv(int wt, const void* W, long long row_bytes, const void* Xq,
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    long long grid = (N + gemv::WARPS - 1) / gemv::WARPS;
-    if (sms > 0 && grid > (long long)sms * (64 / gemv::WARPS)) grid = (long long)sms * (64 / gemv::WARPS);
+    long long grid = (N + gemv::RPC - 1) / gemv::RPC;
+    if (sms > 0 && grid > (long long)sms * 16) grid = (long long)sms * 16;
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const int8_t* xq = static_cast<const int8_t*>(Xq);
     const float2* xds = reinterpret_cast<const float2*>(static_cast<const uint8_t*>(Xq) + M * K);

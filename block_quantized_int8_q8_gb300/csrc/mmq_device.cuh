@@ -276,6 +276,36 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic-serialization attribute may start
+// while the kernel before it in the stream is still running; pdl_wait() returns once that kernel has
+// completed and its memory operations are visible, so every global read and write of the dependent comes
+// after it.  pdl_trigger() lets the next such kernel start (it still waits in its own pdl_wait()).  Both
+// are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Hint: fetch the 128-byte line at p into L2.  Has no effect on what later loads return (L2 is the
+// device's point of coherence), so it may run before pdl_wait().
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Host: launch kernel k with the programmatic-serialization attribute (the kernel calls pdl_wait() before
+// its first global access).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(Params...), dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<Params>(args)...);
+}
+
 // Named barrier over `count` threads (ids other than 0, which __syncthreads uses).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

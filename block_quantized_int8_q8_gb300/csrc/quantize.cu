@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
     const int lane = threadIdx.x & 31, sub = lane & 7, grp = lane >> 3;
     const long long warp_id = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (gridDim.x * (long long)blockDim.x) >> 5;
+    pdl_wait();
+    pdl_trigger();
     // one warp iteration covers 4 groups x QZ_UNROLL blocks
     for (long long base = warp_id * 4 * QZ_UNROLL; base < nblk; base += nwarps * 4 * QZ_UNROLL) {
         float4 v[QZ_UNROLL];
@@ -106,11 +108,10 @@ cudaError_t run_quantize_q8_1(const float* x, long long M, long long K, void* xq
     if (blocks > cap) blocks = cap;
     uint8_t* base = static_cast<uint8_t*>(xq);
     const Q81Layout L = q81_layout(M, K);
-    quantize_q8_1_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+    return launch_pdl(quantize_q8_1_kernel, dim3((unsigned)blocks), dim3(256), s,
         reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(base), reinterpret_cast<float2*>(base + L.ds),
         reinterpret_cast<uint2*>(base + L.h), reinterpret_cast<float*>(base + L.dT),
         reinterpret_cast<float*>(base + L.sT), (int)(K / 32), L.Mp, nblk);
-    return cudaGetLastError();
 }
 
 // Derived sections from existing q8_1 blocks: eight lanes per block, one 32-bit word of codes each.
