@@ -16,6 +16,10 @@
  *   - All buffer pointers are DEVICE pointers owned by the caller.  The library allocates, frees and
  *     synchronises nothing; every call only enqueues kernels on `stream` (0 = the legacy default
  *     stream) and returns.  Buffers must not overlap unless stated.
+ *   - Stream order is kept.  The quantizer and the few-token (M <= 8) product launch as programmatic
+ *     dependents: their CTAs may start while the previous kernel in the stream is still running, but
+ *     they read and write no global memory until it has completed (the few-token kernel only issues L2
+ *     prefetch hints for its weights before that point, which cannot change what any load returns).
  *   - Pointers must be 16-byte aligned.
  *   - Argument errors are reported synchronously as a status code and nothing is enqueued.
  *     Launch failures are reported as MMQ_ERR_CUDA.  Conditions that can only be seen on the device
