@@ -80,6 +80,32 @@ def test_prepare_rebuilds_the_quantizer_shadow():
     _check_shadow(packed, q, d, s, M, K)
 
 
+def test_quantizer_codes_next_to_rounding_boundaries_bit_exact():
+    # every value an f32 neighbour (0..3 ulps either way) of (k + 1/2) * d for its block's own d, so the
+    # quotient x/d sits on or right next to a half-integer: the rounded code must still be that of the
+    # correctly rounded quotient, ties to even; the fp16 shadow must hold the codes' exact bits (+0 for 0)
+    g = np.random.default_rng(29)
+    M, K = 64, 1024
+    amax = (g.uniform(0.5, 2.0, size=(M, K // 32)) * 10.0 ** g.integers(-20, 20, size=(M, 1))).astype(np.float32)
+    d = (amax / np.float32(127)).astype(np.float32)
+    k = g.integers(-127, 127, size=(M, K // 32, 32)).astype(np.float32)
+    x = ((k + np.float32(0.5)) * d[..., None]).astype(np.float32)
+    steps = g.integers(-3, 4, size=x.shape)
+    for _ in range(3):
+        x = np.where(steps > 0, np.nextafter(x, np.float32(np.inf)), np.where(steps < 0, np.nextafter(x, np.float32(-np.inf)), x))
+        steps = steps - np.sign(steps)
+    x[..., 0] = amax                                   # the block's amax, so its d is the one above
+    x = x.reshape(M, K).astype(np.float32)
+    q, dq, s = oracle.quantize_q8_1(x)
+    assert np.array_equal(dq.view(np.uint32), d.view(np.uint32))
+    buf = api.quantize_q8_1(_dev(x))
+    qg, dsg = api.q8_1_views(buf, M, K)
+    assert np.array_equal(qg.cpu().numpy(), q)
+    assert np.array_equal(dsg[..., 1].cpu().numpy().view(np.uint32), s.view(np.uint32))
+    h, _, _ = api.q8_1_shadow_views(buf, M, K)
+    assert np.array_equal(h.cpu().numpy().view(np.uint16), q.astype(np.float16).view(np.uint16))
+
+
 def test_quantizer_extreme_scales_bit_exact():
     g = np.random.default_rng(3)
     x = (g.standard_normal((64, 512)) * 10.0 ** g.integers(-30, 30, size=(64, 1))).astype(np.float32)
