@@ -102,6 +102,7 @@ KERNEL_SOURCES = {
     "mmq_w8a8_tma_kernel": ["gemm_w8a8_tma.cuh", "gemm_tma.cu", "gemm.cuh", "mmq_device.cuh", "internal.h"],
     "mmq_gemm_kernel": ["gemm.cuh", "gemm_q8_0.cu", "gemm_q4_0.cu", "gemm_q4_k.cu", "gemm_iq1_m.cu",
                         "mmq_device.cuh", "internal.h"],
+    "mmvq_kernel": ["gemv.cu", "gemv.h", "gemm.cuh", "mmq_device.cuh", "internal.h"],
 }
 
 
