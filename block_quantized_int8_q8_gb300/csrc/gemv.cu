@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
     constexpr int TSEG = WARPS * CHUNK * TPB;     // terms of one row and token per segment
     static_assert(RPC * MT <= WARPS * 32, "one summing thread per (row, token)");
     __shared__ __align__(16) uint32_t stage[RPC][WARPS][stage_words(WT)];
+    constexpr uint32_t kRowStride = WARPS * stage_words(WT) * 4;   // bytes from stage[r][w] to stage[r + 1][w]
+    constexpr int kUnits16 = chunk_bytes(WT) / 16, kWords = chunk_bytes(WT) / 4;
     __shared__ __align__(16) float terms[RPC][MT][TSEG];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = K / 32, nchunks = (nb + CHUNK - 1) / CHUNK, nseg = (nchunks + WARPS - 1) / WARPS;
@@ -175,17 +177,34 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
             const int nblk = c < nchunks ? min(CHUNK, nb - c * CHUNK) : 0;
             if (nblk > 0) {
                 // every row's chunk c, 16-byte copies that bypass L1 where the rows allow it (the weight
-                // stream then does not evict the activations every row reads)
-                const int words = nblk * chunk_bytes(WT) / 128;              // whole words: K % 256 == 0
+                // stream then does not evict the activations every row reads); the copy loops are unrolled
+                // at compile time over a whole chunk's units and predicated (runtime-bounded loops here
+                // cost more instructions than the decode)
+                const int bytes = nblk * chunk_bytes(WT) / CHUNK;             // whole words: K % 256 == 0
+                const uint8_t* src0 = W + n0 * row_bytes + (long long)c * chunk_bytes(WT);
+                const uint32_t dst0 = smem_u32(stage[0][warp]);
+                if (row16 && (bytes & 15) == 0) {
+                    const int units = bytes >> 4;
 #pragma unroll
-                for (int r = 0; r < RPC; r++) {
-                    if (r < rows) {
-                        const uint8_t* src = W + (n0 + r) * row_bytes + (long long)c * chunk_bytes(WT);
-                        const uint32_t dst = smem_u32(stage[r][warp]);
-                        if (row16 && (words & 3) == 0) {
-                            for (int i = lane; i < words / 4; i += 32) cp_async_16(dst + 16 * i, src + 16 * i, 16);
-                        } else {
-                            for (int i = lane; i < words; i += 32) cp_async_4(dst + 4 * i, src + 4 * i, 4);
+                    for (int r = 0; r < RPC; r++) {
+                        if (r < rows) {
+#pragma unroll
+                            for (int u = 0; u < kUnits16; u += 32) {
+                                const int i = u + lane;
+                                if (i < units) cp_async_16(dst0 + r * kRowStride + 16 * i, src0 + r * row_bytes + 16 * i, 16);
+                            }
+                        }
+                    }
+                } else {
+                    const int words = bytes >> 2;
+#pragma unroll
+                    for (int r = 0; r < RPC; r++) {
+                        if (r < rows) {
+#pragma unroll
+                            for (int u = 0; u < kWords; u += 32) {
+                                const int i = u + lane;
+                                if (i < words) cp_async_4(dst0 + r * kRowStride + 4 * i, src0 + r * row_bytes + 4 * i, 4);
+                            }
                         }
                     }
                 }

@@ -169,6 +169,32 @@ def _extreme_fields(wtype, N, K, g):
     return f
 
 
+@pytest.mark.parametrize("wtype", [synth.Q4_0, synth.Q6_K])
+def test_few_token_chain_reads_what_the_kernels_before_it_wrote(wtype):
+    # the quantizer and the matrix-vector kernel start early as programmatic dependents; each must still
+    # see the previous kernel's writes: layer after layer on one stream, overwrite the weights and the
+    # activations in place with a device copy right before each quantize -> GEMV pair, no host sync
+    # between layers, and every layer's output must equal the oracle's for that layer's inputs
+    M, N, K = 3, 520, 2048
+    layers = [synth.make_problem(wtype, M, N, K, seed=300 + i + wtype) for i in range(4)]
+    src_w = [_dev(pb.W.reshape(-1)) for pb in layers]
+    src_x = [_dev(pb.x) for pb in layers]
+    W = torch.empty_like(src_w[0])
+    x = torch.empty_like(src_x[0])
+    xq = torch.empty(api.q8_1_bytes(M, K), dtype=torch.uint8, device=DEV)
+    outs = [torch.empty((M, N), dtype=torch.float32, device=DEV) for _ in layers]
+    for i in range(len(layers)):
+        W.copy_(src_w[i])
+        x.copy_(src_x[i])
+        api.quantize_q8_1(x, out=xq)
+        api.gemm(wtype, W, xq, M, N, K, out=outs[i])
+    torch.cuda.synchronize()
+    for pb, o in zip(layers, outs):
+        q, d, s = oracle.quantize_q8_1(pb.x)
+        ref = oracle.gemm(wtype, pb.W, q, d, s, N)
+        assert np.array_equal(o.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
 @pytest.mark.parametrize("wtype", BLOCK_TYPES)
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_few_token_path_bit_exact_at_the_bounds(wtype, M):
