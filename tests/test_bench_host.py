@@ -28,12 +28,18 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
 
 
 def test_committed_traffic_matches_the_committed_kernels():
-    # every workload's record in profiles/traffic.json names the kernel bench.py times for it
+    # every workload has a record in profiles/traffic.json naming the kernel bench.py times for it; the
+    # extra records are token-count runs ("<workload>_m<M>", bench.py --tokens M) of the few-token kernel
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
-    assert set(rec) == set(synth.WORKLOADS)
+    assert set(synth.WORKLOADS) <= set(rec)
     for w, ent in rec.items():
-        want = "mmq_w8a8_tma_kernel" if synth.WORKLOADS[w]["wtype"] == synth.W8A8 else "mmq_gemm_tma_kernel"
+        if w in synth.WORKLOADS:
+            want = "mmq_w8a8_tma_kernel" if synth.WORKLOADS[w]["wtype"] == synth.W8A8 else "mmq_gemm_tma_kernel"
+        else:
+            base, _, m = w.rpartition("_m")
+            assert base in synth.WORKLOADS and synth.WORKLOADS[base]["wtype"] != synth.W8A8 and 1 <= int(m) <= 8
+            want = "mmvq_kernel"
         assert ent["kernel"] == want
         assert ent["dram_bytes_per_launch"] > 0
 
