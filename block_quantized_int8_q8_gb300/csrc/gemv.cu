@@ -159,12 +159,17 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
     const bool row16 = (row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(W) & 15) == 0;
     const int sr = threadIdx.x / MT, sm = threadIdx.x % MT;   // summing thread: row sr, token sm
     if ((long long)blockIdx.x * RPC < N) {
-        // the first row group's weights (contiguous rows) into L2 while the kernel before this one finishes
+        // the first segment of the first row group's rows into L2 while the kernel before this one
+        // finishes (whole rows measured slower for the three-segment q6_K rows: the extra prefetches compete
+        // with the previous kernel's traffic)
         const long long n0 = (long long)blockIdx.x * RPC;
-        const long long bytes = min((long long)RPC, N - n0) * row_bytes;
+        const int prow = (int)min(row_bytes, (long long)WARPS * chunk_bytes(WT));   // the first segment
+        const int rows_pf = (int)min((long long)RPC, N - n0);
         const uint8_t* base = W + n0 * row_bytes;
-        for (long long o = (long long)threadIdx.x * 128; o < bytes; o += WARPS * 32 * 128) prefetch_l2(base + o);
-        if (threadIdx.x == 0) prefetch_l2(base + bytes - 1);
+        for (int o = threadIdx.x * 128; o < rows_pf * prow; o += WARPS * 32 * 128) {
+            const int r = o / prow, c = o - r * prow;
+            prefetch_l2(base + r * row_bytes + c);
+        }
     }
     pdl_wait();
     pdl_trigger();
