@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
     pdl_trigger();
     // one warp iteration covers 4 groups x QZ_UNROLL blocks
     for (int base = warp_id * 4 * QZ_UNROLL; base < nblk; base += nwarps * 4 * QZ_UNROLL) {
+        // row and block index of this iteration's first block (one division per iteration; the iteration's
+        // 4 * QZ_UNROLL blocks step forward from it)
+        const int m_base = base / kb, b_base = base - m_base * kb;
         float4 v[QZ_UNROLL];
 #pragma unroll
         for (int u = 0; u < QZ_UNROLL; u++) {
@@ -98,7 +101,11 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
                 if (sub == 0) {
                     const float sv = __fmul_rn(d, (float)sum);
                     ds[blk] = make_float2(d, sv);
-                    const int m = blk / kb, b = blk - m * kb;
+                    int m = m_base, b = b_base + (blk - base);
+                    while (b >= kb) {                  // at most once for rows of 16 blocks or more
+                        b -= kb;
+                        m++;
+                    }
                     dT[b * Mp + m] = d;
                     sT[b * Mp + m] = sv;
                     for (int mm = m + 1; mm < Mp && blk + kb >= nblk; mm++) {   // pad columns: zero
