@@ -195,6 +195,42 @@ def test_few_token_chain_reads_what_the_kernels_before_it_wrote(wtype):
         assert np.array_equal(o.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
+def test_few_token_layers_captured_in_one_cuda_graph():
+    # decode as a CUDA graph: three layers of quantize -> GEMV captured once (programmatic-dependent
+    # launches become graph edges), the input rewritten between replays; each replay must reproduce the
+    # oracle for that input, layer after layer (layer i+1's activations are layer i's output columns)
+    wtype, M, N, K = synth.Q4_0, 2, 1024, 1024
+    layers = [synth.make_problem(wtype, M, N, K, seed=500 + i) for i in range(3)]
+    Ws = [_dev(pb.W.reshape(-1)) for pb in layers]
+    x0 = torch.empty((M, K), dtype=torch.float32, device=DEV)
+    xq = torch.empty(api.q8_1_bytes(M, K), dtype=torch.uint8, device=DEV)
+    outs = [torch.empty((M, N), dtype=torch.float32, device=DEV) for _ in layers]
+
+    def decode():
+        src = x0
+        for W, o in zip(Ws, outs):
+            api.quantize_q8_1(src, out=xq)
+            api.gemm(wtype, W, xq, M, N, K, out=o)
+            src = o                                   # N == K: the next layer reads this output
+    x0.copy_(_dev(layers[0].x))
+    decode()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        decode()
+    for seed in (7, 8):
+        x = np.random.default_rng(seed).standard_normal((M, K), dtype=np.float32)
+        x0.copy_(_dev(x))
+        g.replay()
+        torch.cuda.synchronize()
+        src = x
+        for pb, o in zip(layers, outs):
+            q, d, s = oracle.quantize_q8_1(src)
+            ref = oracle.gemm(wtype, pb.W, q, d, s, N)
+            assert np.array_equal(o.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+            src = ref
+
+
 @pytest.mark.parametrize("wtype", BLOCK_TYPES)
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_few_token_path_bit_exact_at_the_bounds(wtype, M):
