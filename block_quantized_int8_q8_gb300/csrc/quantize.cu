@@ -36,13 +36,24 @@ __device__ __forceinline__ uint2 codes_to_f16x4(int q0, int q1, int q2, int q3) 
     return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
 
+// d = amax / 127, correctly rounded, without a division: q0 = amax * r with r the rounded 1/127, then one
+// correction step q0 + r * (amax - 127 q0) with the residual formed exactly by an FMA (Markstein's
+// correction, "Computation of elementary functions on the IBM RISC System/6000 processor", 1990).  Checked
+// equal to the IEEE quotient for every non-negative finite amax (tests/test_div127_exhaustive.py).
+__device__ __forceinline__ float div127(float a) {
+    constexpr float r = 1.0f / 127.0f;
+    const float q0 = __fmul_rn(a, r);
+    return __fmaf_rn(__fmaf_rn(-q0, 127.0f, a), r, q0);
+}
+
 // The code of x in a block of scale d > 0: round-half-even of the correctly rounded f32 quotient x/d,
-// clamped to [-127, 127].  t = x * (1/d) (both roundings to nearest) lies within |x/d| * 2^-23 (1 + 2^-25)
-// of x/d, and the correctly rounded quotient within |x/d| * 2^-24; for |x/d| <= 127.5 the two differ by
-// less than 2.3e-5.  Rounding to an integer only changes at half-integers, so when t is more than that
-// away from the nearest half-integer, rint(t) is the code the definition gives; otherwise (and when 1/d
-// overflowed: t is then not finite) the quotient is formed exactly.  In: t, x, d; out: the rounded code
-// as a float (an integer in [-127, 127]; a zero code is +0, so its fp16 copy is the integer's).
+// clamped to [-127, 127].  t = x * inv, with inv within 2 ulp of 1/d (__fdividef's bound for normal d),
+// lies within |x/d| * (2^-22 + 2^-24) of x/d, and the correctly rounded quotient within |x/d| * 2^-24; for
+// |x/d| <= 127.5 the two differ by less than 4.6e-5.  Rounding to an integer only changes at
+// half-integers, so when t is more than 1e-4 away from the nearest half-integer, rint(t) is the code the
+// definition gives; otherwise (and for subnormal d, where inv is +inf and t not finite) the quotient is
+// formed exactly.  In: t, x, d; out: the rounded code as a float (an integer in [-127, 127]; a zero code
+// is +0, so its fp16 copy is the integer's).
 __device__ __forceinline__ float q8_code_f(float t, float x, float d) {
     float r = rintf(t);
     if (!(fabsf(t - r) <= 0.4999f)) r = rintf(__fdiv_rn(x, d));
@@ -77,10 +88,10 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-            const float d = __fdiv_rn(a, 127.0f);
+            const float d = div127(a);
             float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
             if (d != 0.0f) {
-                const float inv = __frcp_rn(d);
+                const float inv = d >= 1.17549435e-38f ? __fdividef(1.0f, d) : __int_as_float(0x7f800000);
                 r0 = q8_code_f(__fmul_rn(v[u].x, inv), v[u].x, d);
                 r1 = q8_code_f(__fmul_rn(v[u].y, inv), v[u].y, d);
                 r2 = q8_code_f(__fmul_rn(v[u].z, inv), v[u].z, d);
