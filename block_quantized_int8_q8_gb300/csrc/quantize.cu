@@ -52,12 +52,13 @@ __device__ __forceinline__ float div127(float a) {
 // |x/d| <= 127.5 the two differ by less than 4.6e-5.  Rounding to an integer only changes at
 // half-integers, so when t is more than 1e-4 away from the nearest half-integer, rint(t) is the code the
 // definition gives; otherwise (and for subnormal d, where inv is +inf and t not finite) the quotient is
-// formed exactly.  In: t, x, d; out: the rounded code as a float (an integer in [-127, 127]; a zero code
-// is +0, so its fp16 copy is the integer's).
+// formed exactly.  The clamp to [-127, 127] can only act on that exact path: for a normal d,
+// |x/d| <= 127 / (1 - 2^-24) and |t| stays below 127.5.  In: t, x, d; out: the rounded code as a float
+// (an integer in [-127, 127]; a zero code is +0, so its fp16 copy is the integer's).
 __device__ __forceinline__ float q8_code_f(float t, float x, float d) {
     float r = rintf(t);
-    if (!(fabsf(t - r) <= 0.4999f)) r = rintf(__fdiv_rn(x, d));
-    return __fadd_rn(fminf(127.0f, fmaxf(-127.0f, r)), 0.0f);
+    if (!(fabsf(t - r) <= 0.4999f)) r = fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(x, d))));
+    return __fadd_rn(r, 0.0f);
 }
 
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, uint32_t* __restrict__ q,

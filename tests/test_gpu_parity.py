@@ -106,6 +106,24 @@ def test_quantizer_codes_next_to_rounding_boundaries_bit_exact():
     assert np.array_equal(h.cpu().numpy().view(np.uint16), q.astype(np.float16).view(np.uint16))
 
 
+def test_quantizer_subnormal_scales_bit_exact():
+    # blocks whose amax is so small that d = amax/127 is subnormal (or zero): the codes then come from the
+    # exact quotient and the clamp to [-127, 127] can act; codes, d and s must still equal the oracle's
+    g = np.random.default_rng(17)
+    M, K = 16, 512
+    mags = np.float32(10.0) ** g.integers(-44, -34, size=(M, K // 32, 1)).astype(np.float32)
+    x = (g.uniform(-1.0, 1.0, size=(M, K // 32, 32)).astype(np.float32) * mags).astype(np.float32)
+    x[0, 0] = np.float32(1e-45)                       # the smallest subnormal, repeated
+    x[0, 1] = 0.0
+    x = x.reshape(M, K)
+    q, d, s = oracle.quantize_q8_1(x)
+    assert (d[d > 0] < np.float32(1.17549435e-38)).any()
+    qg, dsg = api.q8_1_views(api.quantize_q8_1(_dev(x)), M, K)
+    assert np.array_equal(qg.cpu().numpy(), q)
+    assert np.array_equal(dsg[..., 0].cpu().numpy().view(np.uint32), d.view(np.uint32))
+    assert np.array_equal(dsg[..., 1].cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
 def test_quantizer_extreme_scales_bit_exact():
     g = np.random.default_rng(3)
     x = (g.standard_normal((64, 512)) * 10.0 ** g.integers(-30, 30, size=(64, 1))).astype(np.float32)
