@@ -10,9 +10,10 @@
 // 4 bytes read per value; 1.25 bytes of q8_1 blocks and 2.25 bytes of shadow (fp16 codes, block-major
 // scales) written.  Eight lanes own one block (one float4 each); amax and sum(q) are warp-shuffle
 // reductions over the eight lanes; every lane stores its four codes as one 32-bit word, so a warp writes
-// 128 contiguous bytes per block quad.  The codes come from x * (1/d) and fall back to the correctly
-// rounded quotient only next to a rounding boundary (q8_code_f): the division was most of the kernel's
-// instructions, and the kernel was issue-bound (21.1 -> 19.2 us for 2048 x 4096 values, bit-identical).
+// 128 contiguous bytes per block quad.  The kernel is issue-bound, so it avoids divisions: d comes from an
+// exact FMA correction step (div127), the codes from x * (1/d) with the correctly rounded quotient formed
+// only next to a rounding boundary (q8_code_f), and the row and column of a block step forward from one
+// division per warp iteration (21.1 -> 16.6 us for 2048 x 4096 values, bit-identical results).
 #include <cstdint>
 #include "internal.h"
 #include <cuda_fp16.h>
