@@ -340,6 +340,8 @@ def setup_workload(name, dev, eager, warmup, flush):
             small = M * pb.ids.shape[1] <= 65536 and pb.experts <= 1024
             moe_tma = K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
             launches_per_step = (4 if small else 7) if moe_tma else 6
+            if M <= 8:
+                launches_per_step = 2       # quantize, matrix-vector kernel reading the ids itself
         else:
             out = torch.empty((M, N), dtype=torch.float32, device=dev)
             # quantize, GEMM (plus the zeroing of the K-split tail tiles' rows on the tile path)
@@ -393,9 +395,10 @@ def setup_workload(name, dev, eager, warmup, flush):
         assert api.read_device_errors() == 0
     tma_path = wt != synth.W8A8 and K % 256 == 0 and (wt != synth.IQ1_M or K % 1024 == 0)
     kernel = "mmq_w8a8_tma_kernel" if wt == synth.W8A8 else ("mmq_gemm_tma_kernel" if tma_path else "mmq_gemm_kernel")
-    if wt != synth.W8A8 and not is_moe and M <= 8:
+    if wt != synth.W8A8 and M <= 8:
         kernel = "mmvq_kernel"
-    return dict(pb=pb, wt=wt, M=M, N=N, K=K, ops=ops, tokens=tokens, x=x, out=out, quant_call=quant_call,
+    return dict(pb=pb, wt=wt, M=M, N=N, K=K, ops=ops, tokens=tokens, x=x, out=out, ids=ids, ws=ws,
+                quant_call=quant_call,
                 gemm_call=gemm_call, run_quant=run_quant, run_gemm=run_gemm, timed_as=timed_as,
                 launches_per_step=launches_per_step, kernel=kernel)
 
@@ -419,15 +422,31 @@ def timed_steps(wl, steps, flush, stream):
     return step_ms, gemm_ms, quant_ms
 
 
+def fewtoken_bytes(wl) -> int:
+    """Algorithmic bytes of one matrix-vector launch: the weight rows it reads (a MoE call reads only the
+    experts its tokens route to), the q8_1 codes and (d, s) pairs of the M tokens, the f32 outputs."""
+    pb, M, N, K = wl["pb"], wl["M"], wl["N"], wl["K"]
+    if pb.ids is not None:
+        w = len(np.unique(pb.ids)) * (pb.W.nbytes // pb.experts)
+        rows = pb.ids.size
+    else:
+        w, rows = pb.W.nbytes, M
+    return int(w + M * K + M * (K // 32) * 8 + rows * N * 4)
+
+
 def decode_stream(wl, dev, stream, replays=20):
     """Few-token (M <= 8) weights as a decode pass sees them: R layers, each its own copy of the weight
-    matrix (R copies together at least twice the L2, so every layer's weights come from HBM), one CUDA graph
-    of R x (quantize, GEMM) replayed `replays` times between two CUDA events; and the same with the GEMMs
-    alone.  No flush is needed: each layer's weights are read once per pass and evicted by the others."""
+    matrix (the bytes R layers read together at least twice the L2, so every layer's weights come from
+    HBM), one CUDA graph of R x (quantize, GEMM) replayed `replays` times between two CUDA events; and the
+    same with the GEMMs alone.  No flush is needed: each layer's weights are read once per pass and evicted
+    by the others.  A MoE layer reads only the experts its tokens route to."""
     import torch
     from block_quantized_int8_q8_gb300 import api
     pb, wt, M, N, K = wl["pb"], wl["wt"], wl["M"], wl["N"], wl["K"]
-    wbytes = wl["pb"].W.nbytes
+    if pb.ids is not None:
+        wbytes = len(np.unique(pb.ids)) * (pb.W.nbytes // pb.experts)
+    else:
+        wbytes = pb.W.nbytes
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (132 << 20)
     R = int(min(128, max(8, -(-(2 * l2) // wbytes))))
     Ws = [torch.from_numpy(pb.W.reshape(-1)).to(dev) for _ in range(R)]
@@ -438,7 +457,10 @@ def decode_stream(wl, dev, stream, replays=20):
         for W in Ws:
             if with_quant:
                 api.quantize_q8_1(x, out=xq)
-            api.gemm(wt, W, xq, M, N, K, out=out)
+            if pb.ids is not None:
+                api.gemm_id(wt, W, pb.experts, xq, wl["ids"], M, N, K, out=out, workspace=wl["ws"])
+            else:
+                api.gemm(wt, W, xq, M, N, K, out=out)
 
     res = {"layers": R, "weight_bytes_per_layer": wbytes, "replays": replays}
     for key, wq in (("layer_us", True), ("gemm_us", False)):
@@ -637,6 +659,14 @@ def main():
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(name, kernel),
                 "peak_source": f"{peak_src} dense bf16 burst (fp16 operands, same nominal rate)",
                 "flops_per_launch": ops}
+    if kernel == "mmvq_kernel":
+        # a few tokens: every weight byte is used M times at most, the kernel is bound by reading them
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        nbytes = fewtoken_bytes(wl)
+        roofline.update(bound="hbm", achieved=nbytes / gemm_avg / 1e9, peak=hbm, unit="GB/s",
+                        frac=nbytes / gemm_avg / 1e9 / hbm, peak_source=f"{peak_src} HBM copy bandwidth",
+                        bytes_per_launch=nbytes)
+        roofline.pop("flops_per_launch")
     int8_peak = ffma = None
     try:
         import ctypes

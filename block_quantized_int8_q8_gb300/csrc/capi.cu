@@ -258,6 +258,14 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
     const IdLayout L = id_layout(M, K, n_slots, n_experts);
     if (!workspace || workspace_bytes < L.total) return MMQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MMQ_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (M <= mmvq_max_m((int)wtype) && M * n_slots <= kMaxGemvPairs) {
+        // a few tokens: each (token, slot) pair is a one-token product with its expert, read straight
+        // from the ids by the matrix-vector kernel (gemv.cu) -- no routing pass, no gather
+        const cudaError_t e = run_gemv_id((int)wtype, W, weight_row_bytes(wtype, K), n_experts, Xq, expert_ids,
+                                          n_slots, out, M, N, K, s);
+        return e == cudaSuccess ? MMQ_OK : cuda_fail(e, "mmq_gemm_id");
+    }
     uint8_t* wb = static_cast<uint8_t*>(workspace);
     RouteWorkspace ws;
     ws.counts = reinterpret_cast<int*>(wb + L.counts);
@@ -267,7 +275,6 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
     ws.work = reinterpret_cast<int*>(wb + L.work);
     ws.rowlist = reinterpret_cast<int*>(wb + L.rowlist);
     ws.max_work = L.max_work;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool tma = tma_gemm_supported((int)wtype, K) && (long long)n_experts * N < (1ll << 31) && L.Rg < (1ll << 31);
     if (!tma && !general_type(wtype)) return MMQ_ERR_UNSUPPORTED;
     cudaError_t e = (tma && route_fused_supported(M, n_slots, n_experts))
@@ -343,7 +350,7 @@ mmq_status mmq_read_device_errors(unsigned* bits, mmq_stream_t stream) {
                                                          read_clear_errors_q8_0,     read_clear_errors_q4_0,
                                                          read_clear_errors_q4_k,     read_clear_errors_iq1_m,
                                                          read_clear_errors_w8a8,     read_clear_errors_tma,
-                                                         read_clear_errors_selftest};
+                                                         read_clear_errors_selftest, read_clear_errors_gemv};
     for (auto r : readers) {
         cudaError_t ei = r(bits, s);
         if (ei != cudaSuccess) e = ei;

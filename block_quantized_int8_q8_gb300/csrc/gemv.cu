@@ -143,11 +143,19 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
 // flight at once: one memory round trip per segment instead of one per chunk), decodes its chunk's blocks
 // (one per lane) and writes each block's f32 term per row and token to shared memory.  Thread t < RPC*MT
 // then adds row t/MT's terms for token t%MT in block order, one dependent chain per (row, token).
-template <int WT, int MT>
-__global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restrict__ W, long long row_bytes,
-                                                        const int8_t* __restrict__ xq,
-                                                        const float2* __restrict__ xds, float* __restrict__ out,
-                                                        int N, int K) {
+//
+// MoE mode (ID): blockIdx.y is one (token, slot) pair of the MUL_MAT_ID product, each a one-token product
+// with its expert's weights: W then holds n_experts matrices of N rows, the pair's expert comes from ids,
+// and the output row is token * slots + slot.  An id outside [0, n_experts) sets MMQ_DEVERR_EXPERT_ID and
+// leaves the row unwritten; a token listing an expert twice sets MMQ_DEVERR_DUP_EXPERT (both rows are
+// still computed), as the routing pass of the tile path does.
+template <int WT, int MT, bool ID = false>
+__global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restrict__ W_, long long row_bytes,
+                                                        const int8_t* __restrict__ xq_,
+                                                        const float2* __restrict__ xds_, float* __restrict__ out_,
+                                                        int N, int K, const int32_t* __restrict__ ids = nullptr,
+                                                        int slots = 1, int n_experts = 1) {
+    static_assert(!ID || MT == 1, "the MoE mode runs one token per (token, slot) pair");
     constexpr int TPB = per16(WT) ? 2 : 1;        // terms per block
     constexpr int TSEG = WARPS * CHUNK * TPB;     // terms of one row and token per segment
     static_assert(RPC * MT <= WARPS * 32, "one summing thread per (row, token)");
@@ -157,9 +165,13 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
     __shared__ __align__(16) float terms[RPC][MT][TSEG];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = K / 32, nchunks = (nb + CHUNK - 1) / CHUNK, nseg = (nchunks + WARPS - 1) / WARPS;
-    const bool row16 = (row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(W) & 15) == 0;
+    const bool row16 = (row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(W_) & 15) == 0;
     const int sr = threadIdx.x / MT, sm = threadIdx.x % MT;   // summing thread: row sr, token sm
-    if ((long long)blockIdx.x * RPC < N) {
+    const uint8_t* W = W_;
+    const int8_t* xq = xq_;
+    const float2* xds = xds_;
+    float* out = out_;
+    if (!ID && (long long)blockIdx.x * RPC < N) {
         // the first segment of the first row group's rows into L2 while the kernel before this one
         // finishes (whole rows measured slower for the three-segment q6_K rows: the extra prefetches compete
         // with the previous kernel's traffic)
@@ -174,6 +186,21 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
     }
     pdl_wait();
     pdl_trigger();
+    if constexpr (ID) {
+        const int pair = blockIdx.y, t = pair / slots, j = pair - t * slots;
+        const int e = ids[pair];
+        if (threadIdx.x == 0 && blockIdx.x == 0) {
+            unsigned err = (e < 0 || e >= n_experts) ? DEVERR_EXPERT_ID : 0u;
+            for (int i = 0; i < j; i++)
+                if (ids[(long long)t * slots + i] == e) err |= DEVERR_DUP_EXPERT;
+            if (err) atomicOr(&g_mmq_device_errors, err);
+        }
+        if (e < 0 || e >= n_experts) return;   // uniform over the CTA
+        W += (long long)e * N * row_bytes;
+        xq += (long long)t * K;
+        xds += (long long)t * (K / 32);
+        out += (long long)pair * N;
+    }
     for (long long g = blockIdx.x; g * RPC < N; g += gridDim.x) {
         const long long n0 = g * RPC;
         const int rows = (int)min((long long)RPC, N - n0);
@@ -303,19 +330,46 @@ template <int WT>
 cudaError_t launch_m(dim3 g, dim3 b, cudaStream_t s, const uint8_t* w, long long row_bytes, const int8_t* xq,
                      const float2* xds, float* out, long long M, long long N, long long K) {
     switch (M) {
-        case 1: return launch_pdl(mmvq_kernel<WT, 1>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
-        case 2: return launch_pdl(mmvq_kernel<WT, 2>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
-        case 3: return launch_pdl(mmvq_kernel<WT, 3>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
-        case 4: return launch_pdl(mmvq_kernel<WT, 4>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
-        case 5: return launch_pdl(mmvq_kernel<WT, 5>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
-        case 6: return launch_pdl(mmvq_kernel<WT, 6>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
-        case 7: return launch_pdl(mmvq_kernel<WT, 7>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
-        case 8: return launch_pdl(mmvq_kernel<WT, 8>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K);
+        case 1: return launch_pdl(mmvq_kernel<WT, 1>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
+        case 2: return launch_pdl(mmvq_kernel<WT, 2>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
+        case 3: return launch_pdl(mmvq_kernel<WT, 3>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
+        case 4: return launch_pdl(mmvq_kernel<WT, 4>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
+        case 5: return launch_pdl(mmvq_kernel<WT, 5>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
+        case 6: return launch_pdl(mmvq_kernel<WT, 6>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
+        case 7: return launch_pdl(mmvq_kernel<WT, 7>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
+        case 8: return launch_pdl(mmvq_kernel<WT, 8>, g, b, s, w, row_bytes, xq, xds, out, (int)N, (int)K, nullptr, 1, 1);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace gemv
+
+cudaError_t run_gemv_id(int wt, const void* W, long long row_bytes, int n_experts, const void* Xq,
+                        const int32_t* ids, int slots, float* out, long long M, long long N, long long K,
+                        cudaStream_t s) {
+    if (M < 1 || M > MMVQ_MAX_M || K % 256 != 0 || slots < 1 || M * slots > kMaxGemvPairs)
+        return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long pairs = M * slots;
+    long long gx = (N + gemv::RPC - 1) / gemv::RPC;
+    const long long cap = sms > 0 ? ((long long)sms * 16 + pairs - 1) / pairs : gx;
+    if (gx > cap) gx = cap > 0 ? cap : 1;
+    const uint8_t* w = static_cast<const uint8_t*>(W);
+    const int8_t* xq = static_cast<const int8_t*>(Xq);
+    const float2* xds = reinterpret_cast<const float2*>(static_cast<const uint8_t*>(Xq) + M * K);
+    const dim3 g((unsigned)gx, (unsigned)pairs), b(gemv::WARPS * 32);
+    const int iN = (int)N, iK = (int)K;
+    switch (wt) {
+        case WT_Q8_0: return launch_pdl(gemv::mmvq_kernel<WT_Q8_0, 1, true>, g, b, s, w, row_bytes, xq, xds, out, iN, iK, ids, slots, n_experts);
+        case WT_Q4_0: return launch_pdl(gemv::mmvq_kernel<WT_Q4_0, 1, true>, g, b, s, w, row_bytes, xq, xds, out, iN, iK, ids, slots, n_experts);
+        case WT_Q4_K: return launch_pdl(gemv::mmvq_kernel<WT_Q4_K, 1, true>, g, b, s, w, row_bytes, xq, xds, out, iN, iK, ids, slots, n_experts);
+        case WT_IQ1_M: return launch_pdl(gemv::mmvq_kernel<WT_IQ1_M, 1, true>, g, b, s, w, row_bytes, xq, xds, out, iN, iK, ids, slots, n_experts);
+        case WT_Q6_K: return launch_pdl(gemv::mmvq_kernel<WT_Q6_K, 1, true>, g, b, s, w, row_bytes, xq, xds, out, iN, iK, ids, slots, n_experts);
+    }
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t run_gemv(int wt, const void* W, long long row_bytes, const void* Xq, float* out, long long M, long long N,
                      long long K, cudaStream_t s) {
@@ -340,5 +394,7 @@ cudaError_t run_gemv(int wt, const void* W, long long row_bytes, const void* Xq,
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
+
+MMQ_DEFINE_ERROR_READER(gemv)
 
 }  // namespace mmq

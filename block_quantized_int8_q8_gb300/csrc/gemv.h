@@ -16,4 +16,13 @@ inline int mmvq_max_m(int) { return MMVQ_MAX_M; }
 cudaError_t run_gemv(int wt, const void* W, long long row_bytes, const void* Xq, float* out, long long M, long long N,
                      long long K, cudaStream_t s);
 
+// Most (token, slot) pairs run_gemv_id takes: one grid row (gridDim.y) per pair.
+constexpr long long kMaxGemvPairs = 65535;
+
+// The same kernel for MUL_MAT_ID at 1 <= M <= MMVQ_MAX_M tokens: W holds n_experts matrices of N rows;
+// out f32 [M][slots][N], row (t, j) the product of token t with expert ids[t][j] (no routing pass).
+cudaError_t run_gemv_id(int wt, const void* W, long long row_bytes, int n_experts, const void* Xq,
+                        const int32_t* ids, int slots, float* out, long long M, long long N, long long K,
+                        cudaStream_t s);
+
 }  // namespace mmq

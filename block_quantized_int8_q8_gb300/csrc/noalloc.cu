@@ -20,6 +20,7 @@
 #include "../../include/mmq.h"
 #include "gemm.cuh"
 #include "internal.h"
+#include "gemv.h"
 
 using namespace mmq;
 
@@ -69,6 +70,13 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
     if (!W || !Xq || !expert_ids || !out) return MMQ_ERR_INVALID_ARG;
     auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (!al(W) || !al(Xq) || !al(out) || !al(expert_ids)) return MMQ_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (M <= mmvq_max_m((int)wtype) && M * n_slots <= kMaxGemvPairs) {
+        // a few tokens: the matrix-vector kernel reads the ids itself and needs no routing lists
+        const cudaError_t e = run_gemv_id((int)wtype, W, weight_row_bytes(wtype, K), n_experts, Xq, expert_ids,
+                                          n_slots, out, M, N, K, s);
+        return e == cudaSuccess ? MMQ_OK : record_cuda_failure(e, "mmq_gemm_id_noalloc");
+    }
 
     // carve the routing lists out of the scratch array (same layout as the mmq_gemm_id workspace)
     const long long rows = M * n_slots;
@@ -90,7 +98,6 @@ extern "C" mmq_status mmq_gemm_id_noalloc(mmq_type wtype, const void* W, int n_e
     ws.work = reinterpret_cast<int*>(sb + work);
     ws.rowlist = reinterpret_cast<int*>(sb + rowlist);
     ws.max_work = max_work;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = run_route(expert_ids, (int)M, n_slots, n_experts, BN, ws, s);
     if (e != cudaSuccess) return record_cuda_failure(e, "mmq_gemm_id_noalloc routing");
 

@@ -179,6 +179,9 @@ mmq_status mmq_gemm_debug_block_sums(mmq_type wtype, const void* W, const void* 
  *              (fp16 codes and block scales, about 2*K + K/4 bytes per (token, slot) row).
  * Routing (count, scan, scatter), the gather and the grouped product run on the device with no host
  * synchronisation.  Out-of-range ids set MMQ_DEVERR_EXPERT_ID and their rows are left unwritten.
+ * For M <= 8 tokens (and M*n_slots <= 65535) the call runs one matrix-vector kernel instead, which reads
+ * the ids itself: each (token, slot) row is a one-token product with its expert, summed in the blockwise
+ * definition's order, and the workspace is not touched (it is still required and checked).
  */
 size_t mmq_gemm_id_workspace_bytes(int64_t M, int64_t K, int n_slots, int n_experts);
 mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void* Xq,
@@ -194,7 +197,8 @@ mmq_status mmq_gemm_id(mmq_type wtype, const void* W, int n_experts, const void*
  * Arguments and results are those of mmq_gemm_id without the workspace.  The routing lists live in a
  * file-scope device array of MMQ_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the
  * library until the process exits; the call itself allocates nothing.  It runs the general kernel on
- * the token rows in place (no gathered copy).  Problems whose routing lists need more than the array
+ * the token rows in place (no gathered copy); for M <= 8 tokens, the matrix-vector kernel of
+ * mmq_gemm_id, which uses no routing lists.  Problems whose routing lists need more than the array
  * (per-expert counts, offsets and cursors, 12 bytes per work item with ceil(M*n_slots/128) + n_experts
  * items, 4 bytes per (token, slot) row, each list rounded up to 256 bytes) are rejected with
  * MMQ_ERR_WORKSPACE.  The first call on each device looks up the array's device

@@ -53,3 +53,18 @@ def test_rescale_ceiling_definition():
     assert bench.rescale_ceiling(synth.Q4_K, ops, 30.0)["fp32_instr_per_element_block"] == 3
     assert bench.rescale_ceiling(synth.W8A8, ops, 30.0) is None
     assert bench.rescale_ceiling(synth.Q4_0, ops, None) is None
+
+
+def test_fewtoken_bytes_counts_only_the_routed_experts():
+    # the few-token roofline's bytes: weight rows read (a MoE call reads only its tokens' experts), the
+    # q8_1 codes and (d, s) pairs of the tokens, the f32 outputs (one row per (token, slot) pair)
+    M, N, K, E = 2, 64, 256, 8
+    pb = synth.make_problem(synth.IQ1_M, M, N, K, seed=3, experts=E, slots=2)
+    ids = pb.ids.copy()
+    ids[:] = [[1, 5], [5, 2]]
+    pb.ids = ids
+    per_expert = N * (K // 256) * 76
+    assert pb.W.nbytes == E * per_expert
+    assert bench.fewtoken_bytes(dict(pb=pb, M=M, N=N, K=K)) == 3 * per_expert + M * K + M * (K // 32) * 8 + 4 * N * 4
+    dense = synth.make_problem(synth.Q4_0, M, N, K, seed=4)
+    assert bench.fewtoken_bytes(dict(pb=dense, M=M, N=N, K=K)) == N * (K // 32) * 18 + M * K + M * (K // 32) * 8 + M * N * 4

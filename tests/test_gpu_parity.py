@@ -465,9 +465,46 @@ def test_gemm_id_skewed_routing():
     assert _rel_err(out, ref) <= TOL
 
 
+@pytest.mark.parametrize("wtype", BLOCK_TYPES)
+@pytest.mark.parametrize("M,E,slots,N,K", [(1, 32, 8, 130, 1280), (3, 8, 4, 257, 2048), (8, 16, 2, 64, 768)])
+def test_few_token_gemm_id_bit_exact(wtype, M, E, slots, N, K):
+    # M <= 8 tokens: each (token, slot) pair runs as a one-token product with its expert on the
+    # matrix-vector kernel, which reads the ids itself (no routing lists); every row equals the oracle's
+    # bit for bit, through both MoE entry points (K = 1280 and 768 end in a partial chunk of blocks)
+    pb = synth.make_problem(wtype, M, N, K, seed=91 + M + wtype, experts=E, slots=slots)
+    q, d, s, xq = _oracle_acts(pb)
+    W, ids = _dev(pb.W.reshape(-1)), _dev(pb.ids)
+    ref = oracle.gemm_id(wtype, pb.W, E, q, d, s, pb.ids, N)
+    api.read_device_errors()
+    out = api.gemm_id(wtype, W, E, xq, ids, M, N, K).cpu().numpy()
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32)), np.abs(out - ref).max()
+    if wtype != synth.Q6_K:
+        out2 = api.gemm_id_noalloc(wtype, W, E, xq, ids, M, N, K).cpu().numpy()
+        assert np.array_equal(out2.view(np.uint32), ref.view(np.uint32))
+    assert api.read_device_errors() == 0
+
+
+def test_few_token_gemm_id_duplicate_ids_flagged_and_computed():
+    # the few-token MoE path checks the routing contract too: a token that lists an expert twice raises
+    # MMQ_DEVERR_DUP_EXPERT and both rows still hold that expert's product
+    wtype, M, E, slots, N, K = synth.IQ1_M, 4, 6, 3, 96, 1024
+    pb = synth.make_problem(wtype, M, N, K, seed=97, experts=E, slots=slots)
+    ids = pb.ids.copy()
+    ids[2, 2] = ids[2, 0]
+    q, d, s, xq = _oracle_acts(pb)
+    api.read_device_errors()
+    out = api.gemm_id(wtype, _dev(pb.W.reshape(-1)), E, xq, _dev(ids), M, N, K).cpu().numpy()
+    bits = api.read_device_errors()
+    assert bits & api.DEVERR_DUP_EXPERT
+    assert not bits & api.DEVERR_EXPERT_ID
+    ref = oracle.gemm_id(wtype, pb.W, E, q, d, s, ids, N)
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+
+
 @pytest.mark.parametrize("bad", ["past_end", "negative"])
-def test_gemm_id_out_of_range_ids_flagged_and_skipped(bad):
-    M, E, slots, N, K = 8, 4, 2, 128, 256
+@pytest.mark.parametrize("M", [8, 40])          # the matrix-vector kernel, then the routed tile path
+def test_gemm_id_out_of_range_ids_flagged_and_skipped(bad, M):
+    E, slots, N, K = 4, 2, 128, 256
     pb = synth.make_problem(synth.Q4_0, M, N, K, seed=71, experts=E, slots=slots)
     ids = pb.ids.copy()
     ids[3, 1] = E + 5 if bad == "past_end" else -1
