@@ -25,4 +25,7 @@ cudaError_t run_gemv_id(int wt, const void* W, long long row_bytes, int n_expert
                         const int32_t* ids, int slots, float* out, long long M, long long N, long long K,
                         cudaStream_t s);
 
+// Read and clear the device error bits the MoE mode raises (mmq_read_device_errors gathers every kernel's).
+cudaError_t read_clear_errors_gemv(unsigned* bits, cudaStream_t s);
+
 }  // namespace mmq

@@ -166,7 +166,6 @@ cudaError_t read_clear_errors_iq1_m(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_w8a8(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_tma(unsigned* bits, cudaStream_t s);
 cudaError_t read_clear_errors_selftest(unsigned* bits, cudaStream_t s);
-cudaError_t read_clear_errors_gemv(unsigned* bits, cudaStream_t s);
 // Device self-test of the bounded waits (selftest.cu): result int32 [4].
 cudaError_t run_wait_timeout_selftest(int* result, cudaStream_t s);
 }  // namespace mmq
