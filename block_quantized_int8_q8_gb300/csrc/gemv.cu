@@ -62,12 +62,15 @@ __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ush
 // (4-bit codes), 32 (6-bit codes) and 9 or 7 (IQ1_M's 8 * code in {0, 8, 16, 24}).
 
 // Decode block j of the staged bytes st: 8 words of int8 values in k order and the scale factors of the
-// blockwise definition (per 32 values, or per 16-value half: wsc[0], wsc[1]).  Super-block types start
-// every record on a 4-byte boundary and read aligned words; Q8_0 and Q4_0 blocks are 2-byte aligned.
+// blockwise definition (per 32 values, or per 16-value half: wsc[0], wsc[1]).  IQ1_M returns 8 * code per
+// byte and the sign bits of its four 8-value groups (gsign); the kernel adds each group's offset.
+// Super-block types start every record on a 4-byte boundary and read aligned words; Q8_0 and Q4_0 blocks
+// are 2-byte aligned.
 template <int WT>
 __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t (&w)[8], float (&wsc)[2],
-                                             float& wmin) {
+                                             float& wmin, uint32_t& gsign) {
     wmin = 0.f;
+    gsign = 0u;
     if constexpr (WT == WT_Q8_0) {                 // f16 d | int8 q[32]
         uint32_t b[9];                             // bytes 34j .. 34j + 35
         st_span<9>(st, 34 * j, b);
@@ -110,14 +113,20 @@ __device__ __forceinline__ void decode_block(const uint32_t* st, int j, uint32_t
 #pragma unroll
         for (int h = 0; h < 2; h++)
             wsc[h] = __fmul_rn(__fmul_rn(d, (float)(2u * (uint32_t)((sbits >> (3 * (2 * sb + h))) & 7u) + 1u)), 0.125f);
-        const uint32_t signs = rec[16] >> (4 * sb);                      // one bit per 8 values
-        const uint32_t cw[2] = {rec[2 * sb], rec[2 * sb + 1]};           // codes of the block's 32 values
+        gsign = (rec[16] >> (4 * sb)) & 15u;                             // one bit per 8 values
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const uint32_t cb = (cw[k >> 2] >> (8 * (k & 3))) & 0xFFu;    // codes of values 4k..4k+3
-            const uint32_t c = (cb & 3u) | ((cb & 0x0Cu) << 6) | ((cb & 0x30u) << 12) | ((cb & 0xC0u) << 18);
-            // 8 * (code - 1) + (+1 | -1), per byte: 8 * code + (-7 | -9) (see bias_byte)
-            w[k] = ((c << 3) + (((signs >> (k >> 1)) & 1u) ? 0x77777777u : 0x79797979u)) ^ 0x80808080u;
+        for (int p = 0; p < 2; p++) {
+            // code word p: byte i holds the 2-bit codes of values 16p + 4i .. + 3 at bits 0-1, 2-3, 4-5,
+            // 6-7; a_t = 8 * code of value 4i + t in byte i, then a byte transpose gives the four words
+            const uint32_t cw = rec[2 * sb + p];
+            const uint32_t a0 = (cw << 3) & 0x18181818u, a1 = (cw << 1) & 0x18181818u;
+            const uint32_t a2 = (cw >> 1) & 0x18181818u, a3 = (cw >> 3) & 0x18181818u;
+            const uint32_t lo01 = __byte_perm(a0, a1, 0x5140), hi01 = __byte_perm(a0, a1, 0x7362);
+            const uint32_t lo23 = __byte_perm(a2, a3, 0x5140), hi23 = __byte_perm(a2, a3, 0x7362);
+            const uint32_t v[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                                   __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+#pragma unroll
+            for (int i = 0; i < 4; i++) w[4 * p + i] = v[i];           // 8 * code (the kernel adds k_g * S_g)
         }
     } else {                                        // q6_K: int8 sc[16] | f16 d | pad | four 48 B records
         const uint32_t* rec = st + 56 * (j >> 3);  // 224-byte records
@@ -259,6 +268,21 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
             // Q4_0 codes stay unsigned (0..15): the block dot is sum(code * q) - 8 * sum(q), exact in int32,
             // with 8 * sum(q) formed once per token and shared by the group's rows
             int sq8[MT];
+            // IQ1_M, one or two tokens: a value is 8 * code + k_g, k_g = -9 (sign bit of group g set) or
+            // -7, so the block dot is dp4a(8 * code, q) + sum_g k_g * S_g with S_g the token's sum over
+            // group g, formed once per token and shared by the rows.  More tokens would hold 4 sums each;
+            // there the rows add k_g per byte once instead (measured: the sums cost registers from 3 tokens)
+            int gs[WT == WT_IQ1_M && MT <= 2 ? MT : 1][4];
+            if constexpr (WT == WT_IQ1_M && MT <= 2) {
+#pragma unroll
+                for (int m = 0; m < MT; m++) {
+                    const int e1 = 0x01010101;
+                    gs[m][0] = __dp4a(e1, x0[m].y, __dp4a(e1, x0[m].x, 0));
+                    gs[m][1] = __dp4a(e1, x0[m].w, __dp4a(e1, x0[m].z, 0));
+                    gs[m][2] = __dp4a(e1, x1[m].y, __dp4a(e1, x1[m].x, 0));
+                    gs[m][3] = __dp4a(e1, x1[m].w, __dp4a(e1, x1[m].z, 0));
+                }
+            }
 #pragma unroll
             for (int m = 0; m < MT; m++) {
                 int t = 0;
@@ -283,7 +307,18 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
                     if (r >= rows) break;
                     uint32_t w[8];
                     float wsc[2], wmin;
-                    decode_block<WT>(stage[r][warp], lane, w, wsc, wmin);
+                    uint32_t gsign;
+                    decode_block<WT>(stage[r][warp], lane, w, wsc, wmin, gsign);
+                    // IQ1_M: value = 8 * code + k_g, k_g = -9 for a set sign bit of group g, else -7
+                    int kg[4] = {0, 0, 0, 0};
+                    if constexpr (WT == WT_IQ1_M && MT <= 2) {
+#pragma unroll
+                        for (int g4 = 0; g4 < 4; g4++) kg[g4] = ((gsign >> g4) & 1u) ? -9 : -7;
+                    } else if constexpr (WT == WT_IQ1_M) {
+#pragma unroll
+                        for (int k = 0; k < 8; k++)     // 8 * code + (-7 | -9) per byte (see bias_byte)
+                            w[k] = (w[k] + (((gsign >> (k >> 1)) & 1u) ? 0x77777777u : 0x79797979u)) ^ 0x80808080u;
+                    }
 #pragma unroll
                     for (int m = 0; m < MT; m++) {
                         int I0 = 0, I1 = WT == WT_Q4_0 ? -sq8[m] : 0;
@@ -295,6 +330,10 @@ __global__ void __launch_bounds__(WARPS * 32) mmvq_kernel(const uint8_t* __restr
                         I1 = __dp4a((int)w[5], x1[m].y, I1);
                         I1 = __dp4a((int)w[6], x1[m].z, I1);
                         I1 = __dp4a((int)w[7], x1[m].w, I1);
+                        if constexpr (WT == WT_IQ1_M && MT <= 2) {
+                            I0 += kg[0] * gs[m][0] + kg[1] * gs[m][1];
+                            I1 += kg[2] * gs[m][2] + kg[3] * gs[m][3];
+                        }
                         float* tp = &terms[r][m][(warp * CHUNK + lane) * TPB];
                         if constexpr (per16(WT)) {
                             tp[0] = __fmul_rn(__fmul_rn(ds[m].x, wsc[0]), (float)I0);
