@@ -91,6 +91,13 @@ def test_quantize_and_gemm_id_validation(lib):
     assert lib.mmq_gemm_id(*ok, None, need, None) == 6
     assert lib.mmq_gemm_id(api.W8A8, *ok[1:], FAKE, need, None) == 4
     assert lib.mmq_gemm_id(api.IQ1_M, FAKE, 0, *ok[3:], FAKE, need, None) == 1
+    # four tokens take the matrix-vector kernel, which uses no workspace; the contract still checks it
+    few = (api.Q4_0, FAKE, 4, FAKE, FAKE, 2, FAKE, 4, 128, 256)
+    need4 = api.gemm_id_workspace_bytes(4, 256, 2, 4)
+    assert lib.mmq_gemm_id(*few, FAKE, need4 - 1, None) == 6
+    assert lib.mmq_gemm_id(*few, None, need4, None) == 6
+    assert lib.mmq_gemm_id(*few, FAKE + 8, need4, None) == 3
+    assert lib.mmq_gemm_id(api.Q4_0, FAKE, 4, FAKE, FAKE, 2, FAKE, 4, 128, 96, FAKE, need4, None) == 2
     assert lib.mmq_gemm_debug_partials(api.Q4_K, FAKE, FAKE, FAKE, 4, 4, 128, None) == 2
     assert lib.mmq_gemm_debug_partials(api.Q6_K, FAKE, FAKE, FAKE, 4, 4, 256, None) == 4   # TMA kernel only
     assert lib.mmq_gemm(6, FAKE, FAKE, FAKE, 4, 4, 256, None) == 1                         # unknown type
