@@ -466,11 +466,13 @@ def test_gemm_id_skewed_routing():
 
 
 @pytest.mark.parametrize("wtype", BLOCK_TYPES)
-@pytest.mark.parametrize("M,E,slots,N,K", [(1, 32, 8, 130, 1280), (3, 8, 4, 257, 2048), (8, 16, 2, 64, 768)])
+@pytest.mark.parametrize("M,E,slots,N,K", [(1, 32, 8, 130, 1280), (3, 8, 4, 257, 2048), (8, 16, 2, 64, 768),
+                                           (8, 8, 8, 96, 512), (8, 16, 9, 96, 512)])
 def test_few_token_gemm_id_bit_exact(wtype, M, E, slots, N, K):
     # M <= 8 tokens: each (token, slot) pair runs as a one-token product with its expert on the
     # matrix-vector kernel, which reads the ids itself (no routing lists); every row equals the oracle's
-    # bit for bit, through both MoE entry points (K = 1280 and 768 end in a partial chunk of blocks)
+    # bit for bit, through both MoE entry points (K = 1280 and 768 end in a partial chunk of blocks; every
+    # token routed to all 8 experts; 9 slots per token)
     pb = synth.make_problem(wtype, M, N, K, seed=91 + M + wtype, experts=E, slots=slots)
     q, d, s, xq = _oracle_acts(pb)
     W, ids = _dev(pb.W.reshape(-1)), _dev(pb.ids)
