@@ -388,13 +388,10 @@ cudaError_t run_gemv_id(int wt, const void* W, long long row_bytes, int n_expert
                         cudaStream_t s) {
     if (M < 1 || M > MMVQ_MAX_M || K % 256 != 0 || slots < 1 || M * slots > kMaxGemvPairs)
         return cudaErrorInvalidValue;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long pairs = M * slots;
-    long long gx = (N + gemv::RPC - 1) / gemv::RPC;
-    const long long cap = sms > 0 ? ((long long)sms * 16 + pairs - 1) / pairs : gx;
-    if (gx > cap) gx = cap > 0 ? cap : 1;
+    // one CTA per (row group, pair), no grid-stride rounds: capping the grid at 16 CTAs per SM (as the
+    // dense launch does) measured 10 % slower for 8 pairs of 384 row groups
+    const long long gx = (N + gemv::RPC - 1) / gemv::RPC;
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const int8_t* xq = static_cast<const int8_t*>(Xq);
     const float2* xds = reinterpret_cast<const float2*>(static_cast<const uint8_t*>(Xq) + M * K);
