@@ -68,3 +68,62 @@ def test_fewtoken_bytes_counts_only_the_routed_experts():
     assert bench.fewtoken_bytes(dict(pb=pb, M=M, N=N, K=K)) == 3 * per_expert + M * K + M * (K // 32) * 8 + 4 * N * 4
     dense = synth.make_problem(synth.Q4_0, M, N, K, seed=4)
     assert bench.fewtoken_bytes(dict(pb=dense, M=M, N=N, K=K)) == N * (K // 32) * 18 + M * K + M * (K // 32) * 8 + M * N * 4
+
+
+def test_workload_ops_count_every_routed_row_and_config_names_the_routing():
+    ops, tokens = bench.workload_ops("iq1_m_moe")
+    w = synth.WORKLOADS["iq1_m_moe"]
+    assert tokens == w["M"] and ops == 2.0 * w["M"] * w["slots"] * w["N"] * w["K"]
+    cfg = bench.workload_config("iq1_m_moe")
+    assert cfg["experts"] == w["experts"] and cfg["slots"] == w["slots"] and cfg["wtype"] == "IQ1_M"
+    assert "experts" not in bench.workload_config("q4_0_7b")
+    # weak scaling: every rank does a step's units; the job rate is over the slowest rank's time
+    assert bench.job_throughput(10.0, 4, 3, 2.0) == 60.0
+
+
+class _FakeProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def test_clock_record_keeps_the_timed_window_and_reports_throttle_reasons(tmp_path):
+    # nvidia-smi lines: timestamp, sm, max sm, power, active mask, hw_slowdown, hw_thermal, sw_thermal,
+    # sw_power_cap; the first and last samples fall outside the timed window and are dropped
+    lines = [
+        "2026/01/02 10:00:00.000, 900 MHz, 2070 MHz, 120.0 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/02 10:00:01.000, 2070 MHz, 2070 MHz, 900.5 W, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/01/02 10:00:01.020, 2040 MHz, 2070 MHz, 910.0 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/02 10:00:01.040, 2055 MHz, 2070 MHz, 905.0 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/02 10:00:05.000, 600 MHz, 2070 MHz, 100.0 W, 0x8, Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    import datetime
+    ts = lambda s: datetime.datetime.strptime(s, "%Y/%m/%d %H:%M:%S.%f").timestamp()   # noqa: E731
+    cs = bench.ClockSampler("0")
+    cs.path = str(tmp_path / "clocks.csv")
+    with open(cs.path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    cs.out = open(cs.path, "a")
+    cs.proc = _FakeProc()
+    cs.mark(ts("2026/01/02 10:00:01.000"), ts("2026/01/02 10:00:01.040"))
+    rec = cs.stop()
+    assert rec["samples"] == 3
+    assert rec["sm_mhz"] == 2055.0 and rec["sm_max_mhz"] == 2070.0 and rec["power_w_max"] == 910.0
+    assert rec["reasons"] == ["sw_power_cap"]          # the hw_slowdown sample lies outside the window
+
+
+def test_clock_record_without_nvidia_smi_says_so():
+    rec = bench.ClockSampler("0").stop()
+    assert rec["samples"] == 0 and rec["sm_mhz"] is None and rec["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_cpu_baseline_is_the_oracle_on_a_bounded_sample():
+    pb = synth.workload("q8_0_tiny")
+    rec = bench.cpu_baseline(pb, "q8_0_tiny", target_s=0.3)
+    assert rec["kind"] == "oracle" and rec["unit"] == "TOPS" and rec["cores"] >= 1 and rec["value"] > 0
+    n = int(rec["sample"].split(" of ")[0])
+    assert 1 <= n <= pb.M and f"of {pb.M} token rows of q8_0_tiny" in rec["sample"]
+    assert rec["tok_per_s"] > 0
