@@ -95,7 +95,7 @@ typedef enum {
     MMQ_ERR_INVALID_ARG = 1,   /* null pointer, unknown type, negative size */
     MMQ_ERR_SHAPE = 2,         /* K (or M, N) violates the shape rules above */
     MMQ_ERR_ALIGN = 3,         /* a pointer is not 16-byte aligned */
-    MMQ_ERR_UNSUPPORTED = 4,   /* valid request this build does not implement */
+    MMQ_ERR_UNSUPPORTED = 4,   /* valid request the library does not implement */
     MMQ_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
     MMQ_ERR_WORKSPACE = 6      /* workspace pointer null or smaller than required */
 } mmq_status;
