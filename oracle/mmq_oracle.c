@@ -511,9 +511,14 @@ int oracle_gemm_id(int wtype, const uint8_t* W, int64_t n_experts, const int8_t*
         for (int64_t i = 0; i < M * n_slots; i++) {
             if (ids[i] != e) continue;
             int64_t t = i / n_slots;
+#ifdef MUT_MOE_SLOT_MAJOR
+            const int64_t orow = (i % n_slots) * M + t;      /* output rows slot-major instead of token-major */
+#else
+            const int64_t orow = i;
+#endif
             for (int64_t n = 0; n < N; n++)
-                out[i * N + n] = block_dot_row(wtype, xq + t * K, xd + t * nb, xs + t * nb, wq + n * K,
-                                               wsc + n * (K / G), wmin + n * nb, K);
+                out[orow * N + n] = block_dot_row(wtype, xq + t * K, xd + t * nb, xs + t * nb, wq + n * K,
+                                                  wsc + n * (K / G), wmin + n * nb, K);
         }
     }
     free(wq); free(wsc); free(wmin);
