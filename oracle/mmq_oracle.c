@@ -118,7 +118,11 @@ int oracle_quantize_q8_1(const float* x, int64_t M, int64_t K, int8_t* q, float*
                 float a = fabsf(xb[i]);
                 if (a > amax) amax = a;
             }
+#ifdef MUT_SCALE_RECIP
+            float db = amax * (1.0f / 127.0f);              /* d from a rounded reciprocal */
+#else
             float db = amax / 127.0f;
+#endif
             int32_t sum = 0;
             for (int i = 0; i < 32; i++) {
                 int32_t qi = 0;
