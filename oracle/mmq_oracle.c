@@ -96,7 +96,12 @@ static uint16_t float_to_bf16_rne(float f) {
     memcpy(&u, &f, 4);
     if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
     uint32_t lsb = (u >> 16) & 1u;
+#ifdef MUT_BF16_HALF_UP
+    u += 0x8000u;                                           /* ties rounded up instead of to even */
+    (void)lsb;
+#else
     u += 0x7FFFu + lsb;
+#endif
     return (uint16_t)(u >> 16);
 }
 
@@ -140,7 +145,15 @@ int oracle_quantize_q8_1(const float* x, int64_t M, int64_t K, int8_t* q, float*
                 sum += qi;
             }
             d[m * nb + b] = db;
+#ifdef MUT_SUM_ORDER
+            {   /* s as a running f32 sum of d*q instead of d times the exact integer sum */
+                float acc = 0.0f;
+                for (int i = 0; i < 32; i++) acc += db * (float)q[m * K + b * 32 + i];
+                s[m * nb + b] = acc;
+            }
+#else
             s[m * nb + b] = db * (float)sum;
+#endif
         }
     }
     return 0;
@@ -398,7 +411,11 @@ static float block_dot_row(int wtype, const int8_t* xq, const float* xd, const f
 #ifndef MUT_DROP_MIN
             if (wtype == OR_Q4_K) {
                 float v = wmin[b] * xs[b];
+#ifdef MUT_MIN_SIGN
+                u = u + v;                                  /* min term added instead of subtracted */
+#else
                 u = u - v;
+#endif
             }
 #endif
             acc = acc + u;
