@@ -127,3 +127,21 @@ def test_cpu_baseline_is_the_oracle_on_a_bounded_sample():
     n = int(rec["sample"].split(" of ")[0])
     assert 1 <= n <= pb.M and f"of {pb.M} token rows of q8_0_tiny" in rec["sample"]
     assert rec["tok_per_s"] > 0
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    # the reference arm times the oracle on the host; under torchrun the other ranks exit 0 without work
+    import subprocess
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "q8_0_tiny",
+           "--steps", "2", "--warmup", "3"]
+    r1 = subprocess.run(cmd, env=dict(os.environ, RANK="1", WORLD_SIZE="2"), capture_output=True, text=True,
+                        timeout=300)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    r0 = subprocess.run(cmd, env=dict(os.environ, RANK="0"), capture_output=True, text=True, timeout=300)
+    assert r0.returncode == 0
+    line = json.loads(r0.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "q8_0_tiny" and line["higher_is_better"] is True
