@@ -149,6 +149,10 @@ mmq_status mmq_q8_1_prepare(void* xq, int64_t M, int64_t K, mmq_stream_t stream)
  * Block types: out[m,n] = sum_b scale_b * I_b with the exact int32 block dot I_b and the f32 scale
  * products of the layouts above (Q4_K adds -dmin*m_b*s[m,b]; IQ1_M has per-16 scales d(2s+1)/8).
  * W8A8: I = exact int32 dot over the full K, out = bf16_rne(((float)I * xs[m]) * ws[n]).
+ * Summation order: for M <= 8 tokens (block types) the block terms are added in block order, so out equals
+ * the blockwise definition evaluated in that order bit for bit; larger M runs on the tensor-core kernels,
+ * which may add them in another f32 order (and, for K split over CTAs, with atomics), within 1e-3 of the
+ * output scale.  W8A8 is bit-exact at every M.
  */
 mmq_status mmq_gemm(mmq_type wtype, const void* W, const void* Xq, void* out,
                     int64_t M, int64_t N, int64_t K, mmq_stream_t stream);
